@@ -1,0 +1,80 @@
+// Internal types and helpers shared by the libdwconv kernels (not installed).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+
+#include "dwconv.h"
+
+namespace dwconv {
+
+// Validated convolution geometry, passed to kernels by value.
+struct Conv {
+  int64_t N, C, H, W;
+  int m, kh, kw, sh, sw, ph, pw, dh, dw;
+  int64_t Ho, Wo;
+  int64_t off, ctot;  // channel slice of y / gy
+  int dtype;
+
+  __host__ __device__ int64_t OC() const { return C * m; }
+  __host__ __device__ int64_t x_plane() const { return H * W; }
+  __host__ __device__ int64_t y_plane() const { return Ho * Wo; }
+  // element offset of plane (n, oc) in y / gy
+  __host__ __device__ int64_t y_base(int64_t n, int64_t oc) const {
+    return (n * ctot + off + oc) * Ho * Wo;
+  }
+  __host__ __device__ int64_t x_base(int64_t n, int64_t c) const {
+    return (n * C + c) * H * W;
+  }
+};
+
+// ---- storage type <-> fp32 -------------------------------------------------
+template <typename T> __device__ __forceinline__ float ld(const T* p);
+template <> __device__ __forceinline__ float ld<float>(const float* p) { return __ldg(p); }
+template <> __device__ __forceinline__ float ld<__half>(const __half* p) { return __half2float(__ldg(p)); }
+template <> __device__ __forceinline__ float ld<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat162float(__ldg(p));
+}
+
+template <typename T> __device__ __forceinline__ float to_f(T v);
+template <> __device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f<__half>(__half v) { return __half2float(v); }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ __half from_f<__half>(float v) { return __float2half_rn(v); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+// plain (coherent) load for data this kernel may also write
+template <typename T> __device__ __forceinline__ float ld_rw(const T* p) { return to_f<T>(*p); }
+
+inline int div_up(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+
+// Launch helpers: each family exposes launch functions templated on nothing;
+// dtype dispatch happens inside.
+#define DWCONV_DISPATCH_DTYPE(dt, T, ...)                        \
+  switch (dt) {                                                  \
+    case DWCONV_F32: { using T = float; __VA_ARGS__; } break;    \
+    case DWCONV_F16: { using T = __half; __VA_ARGS__; } break;   \
+    case DWCONV_BF16: { using T = __nv_bfloat16; __VA_ARGS__; } break; \
+    default: break;                                              \
+  }
+
+// ---- kernel families (each returns cudaGetLastError() after its launches) --
+// generic.cu: correct for every valid descriptor, one output per thread.
+cudaError_t fwd_generic(const Conv& c, const void* x, const void* w, const void* b, void* y,
+                        cudaStream_t s);
+cudaError_t bwd_data_generic(const Conv& c, const void* gy, const void* w, void* gx,
+                             bool accumulate, cudaStream_t s);
+// pass 1 writes ws[chunk][oc][taps + 1] (last slot = bias) for `chunks` batch chunks.
+cudaError_t bwd_weight_generic_pass1(const Conv& c, const void* x, const void* gy, float* ws,
+                                     int chunks, bool want_w, bool want_b, cudaStream_t s);
+cudaError_t bwd_weight_pass2(const Conv& c, const float* ws, int chunks, void* gw, void* gb,
+                             cudaStream_t s);
+
+}  // namespace dwconv

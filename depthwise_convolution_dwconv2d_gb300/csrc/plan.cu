@@ -1,0 +1,95 @@
+// Shape planner: picks a kernel family per pass from the descriptor alone,
+// so a descriptor always maps to the same kernels (and the same bwd_weight
+// workspace size). DWCONV_FORCE_ALGO=generic pins every pass to the generic
+// kernels (used by the tests to cross-check the tiled ones).
+#include <cstdlib>
+#include <cstring>
+
+#include "plan.h"
+
+namespace dwconv {
+namespace {
+
+bool force_generic() {
+  const char* e = std::getenv("DWCONV_FORCE_ALGO");
+  return e && std::strcmp(e, "generic") == 0;
+}
+
+}  // namespace
+
+const char* algo_name(Algo a) {
+  switch (a) {
+    case Algo::Generic: return "generic";
+    case Algo::Tile: return "tile";
+    case Algo::Large: return "large";
+  }
+  return "unknown";
+}
+
+Algo plan_fwd(const Conv& c) {
+  if (force_generic()) return Algo::Generic;
+  return Algo::Generic;
+}
+
+Algo plan_bwd_data(const Conv& c) {
+  if (force_generic()) return Algo::Generic;
+  return Algo::Generic;
+}
+
+WPlan plan_bwd_weight(const Conv& c) {
+  // generic first pass: a chunk of whole samples per block, at most 2^20
+  // positions per chunk so each thread's serial chain stays <= 4096 terms.
+  const int64_t hw = c.Ho * c.Wo;
+  int64_t nb = (int64_t(1) << 20) / hw;
+  if (nb < 1) nb = 1;
+  if (nb > c.N) nb = c.N > 0 ? c.N : 1;
+  int64_t chunks = c.N > 0 ? (c.N + nb - 1) / nb : 1;
+  if (chunks > 65535) chunks = 65535;
+  return WPlan{Algo::Generic, (int)chunks};
+}
+
+cudaError_t run_fwd(Algo a, const Conv& c, const void* x, const void* w, const void* b, void* y,
+                    cudaStream_t s) {
+  switch (a) {
+    default: return fwd_generic(c, x, w, b, y, s);
+  }
+}
+
+cudaError_t run_bwd_data(Algo a, const Conv& c, const void* gy, const void* w, void* gx,
+                         bool accumulate, cudaStream_t s) {
+  switch (a) {
+    default: return bwd_data_generic(c, gy, w, gx, accumulate, s);
+  }
+}
+
+cudaError_t run_bwd_weight(const WPlan& p, const Conv& c, const void* x, const void* gy, void* gw,
+                           void* gb, float* ws, cudaStream_t s) {
+  cudaError_t e;
+  switch (p.algo) {
+    default:
+      e = bwd_weight_generic_pass1(c, x, gy, ws, p.chunks, gw != nullptr, gb != nullptr, s);
+      break;
+  }
+  if (e != cudaSuccess) return e;
+  return bwd_weight_pass2(c, ws, p.chunks, gw, gb, s);
+}
+
+cudaError_t run_fwd_multi(int nb, const Conv* cs, const void* x, const void* const* w,
+                          const void* const* bias, void* y, cudaStream_t s) {
+  for (int i = 0; i < nb; ++i) {
+    cudaError_t e = run_fwd(plan_fwd(cs[i]), cs[i], x, w[i], bias ? bias[i] : nullptr, y, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t run_bwd_data_multi(int nb, const Conv* cs, const void* gy, const void* const* w,
+                               void* gx, cudaStream_t s) {
+  for (int i = 0; i < nb; ++i) {
+    cudaError_t e = run_bwd_data(plan_bwd_data(cs[i]), cs[i], gy, w[i], gx, i > 0, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace dwconv

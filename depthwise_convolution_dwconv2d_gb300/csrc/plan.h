@@ -1,0 +1,37 @@
+// Kernel-family planner and dispatch (internal to libdwconv).
+#pragma once
+
+#include "common.cuh"
+
+namespace dwconv {
+
+constexpr int kMaxBranches = 8;
+
+enum class Algo {
+  Generic = 0,   // generic.cu: any shape
+  Tile = 1,      // tile_fwd.cu / tile_bwd.cu: register-blocked smem tiles, small kernels
+  Large = 2,     // large.cu: large-kernel direct convolution
+};
+
+struct WPlan {
+  Algo algo;
+  int chunks;    // batch chunks of the first bwd_weight pass
+};
+
+const char* algo_name(Algo a);
+Algo plan_fwd(const Conv& c);
+Algo plan_bwd_data(const Conv& c);
+WPlan plan_bwd_weight(const Conv& c);
+
+cudaError_t run_fwd(Algo a, const Conv& c, const void* x, const void* w, const void* b, void* y,
+                    cudaStream_t s);
+cudaError_t run_bwd_data(Algo a, const Conv& c, const void* gy, const void* w, void* gx,
+                         bool accumulate, cudaStream_t s);
+cudaError_t run_bwd_weight(const WPlan& p, const Conv& c, const void* x, const void* gy, void* gw,
+                           void* gb, float* ws, cudaStream_t s);
+cudaError_t run_fwd_multi(int nb, const Conv* cs, const void* x, const void* const* w,
+                          const void* const* bias, void* y, cudaStream_t s);
+cudaError_t run_bwd_data_multi(int nb, const Conv* cs, const void* gy, const void* const* w,
+                               void* gx, cudaStream_t s);
+
+}  // namespace dwconv

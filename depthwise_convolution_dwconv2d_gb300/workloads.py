@@ -1,0 +1,136 @@
+"""Synthetic workloads: layer shapes and input recipes (no convolution arithmetic).
+
+The shapes stand in for the workloads the pages time:
+  * "pr1"        -- the smallest MobileNet-style layer of "Spatial Depthwise
+                    Convolution on the GPU #3057" (N=1, C=32, 28x28, 3x3);
+  * "mobilenet"  -- the MobileNet layer table of that PR at batch 64
+                    (3x3, pad 1, stride 1 or 2), fp32;
+  * "largek"     -- the MegEngine large-kernel depthwise article's setting
+                    (section "Running time": batch 64, 384 channels) with
+                    square kernels 7..31 on 32/48/64 inputs, fp32 and fp16;
+  * "multidil"   -- the DynamicConvolutionOperator's fused dilation 1/3/5
+                    branches (dim 64, resolution 256, batch 2), bf16,
+                    stored into one concatenated output;
+  * "multiplier" -- a depth-multiplier-2 5x5 training layer with bias, bf16.
+No public dataset is involved: every tensor is drawn by ``synth`` with seed 0
+and per-tensor streams. Variances are read as variances: N(0, 1/9) has
+standard deviation 1/3.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+from . import synth
+
+
+@dataclass
+class Layer:
+    N: int
+    C: int
+    H: int
+    W: int
+    k: int = 3
+    s: int = 1
+    p: int = 1
+    d: int = 1
+    m: int = 1
+    bias: bool = False
+    dtype: str = "f32"
+    x_dist: str = "uniform"   # "uniform" = U[-1, 1], "normal" = N(0, 1)
+    w_std: float | None = None  # default 1/k
+    b_std: float = math.sqrt(0.1)
+    name: str = ""
+
+    @property
+    def OC(self):
+        return self.C * self.m
+
+    @property
+    def Ho(self):
+        return (self.H + 2 * self.p - self.d * (self.k - 1) - 1) // self.s + 1
+
+    @property
+    def Wo(self):
+        return (self.W + 2 * self.p - self.d * (self.k - 1) - 1) // self.s + 1
+
+    def desc_kwargs(self):
+        return dict(N=self.N, C=self.C, H=self.H, W=self.W, kernel=self.k, stride=self.s,
+                    pad=self.p, dilation=self.d, multiplier=self.m, dtype=self.dtype)
+
+    def label(self):
+        return self.name or (f"N{self.N}C{self.C}H{self.H}k{self.k}s{self.s}d{self.d}"
+                             f"m{self.m}{'b' if self.bias else ''}_{self.dtype}")
+
+
+@dataclass
+class Multi:
+    """Several branches over one input writing one concatenated output."""
+    N: int
+    C: int
+    H: int
+    W: int
+    dilations: tuple = (1, 3, 5)
+    k: int = 3
+    dtype: str = "bf16"
+    x_dist: str = "normal"
+    w_std: float = 1.0 / 3.0
+    name: str = "multidil"
+
+    def branches(self):
+        nb = len(self.dilations)
+        return [Layer(N=self.N, C=self.C, H=self.H, W=self.W, k=self.k, s=1, p=d * (self.k // 2),
+                      d=d, dtype=self.dtype, x_dist=self.x_dist, w_std=self.w_std)
+                for d in self.dilations], nb * self.C
+
+    def label(self):
+        return self.name
+
+
+def mobilenet(N=64):
+    layers = [(64, 112, 2), (128, 56, 1), (128, 56, 2), (256, 28, 1), (256, 28, 2),
+              (512, 14, 1), (512, 14, 2), (1024, 7, 2)]
+    return [Layer(N=N, C=c, H=h, W=h, k=3, s=s, p=1, name=f"mb_C{c}_H{h}_s{s}") for c, h, s in layers]
+
+
+def pr1():
+    return [Layer(N=1, C=32, H=28, W=28, k=3, s=1, p=1, name="pr1_C32_H28")]
+
+
+def largek(N=64, C=384, sizes=(32, 48, 64), ks=(7, 13, 21, 27, 31), dtypes=("f32", "f16")):
+    return [Layer(N=N, C=C, H=h, W=h, k=k, s=1, p=k // 2, dtype=dt, name=f"lk_H{h}_k{k}_{dt}")
+            for dt in dtypes for h in sizes for k in ks]
+
+
+def multidil(N=2, C=64, H=256):
+    return Multi(N=N, C=C, H=H, W=H)
+
+
+def multiplier(N=128):
+    return [Layer(N=N, C=256, H=28, W=28, k=5, s=1, p=2, m=2, bias=True, dtype="bf16",
+                  x_dist="normal", w_std=1.0 / 5.0, name="mult_C256_H28_k5_m2")]
+
+
+@dataclass
+class Inputs:
+    x: synth.Tensor
+    w: synth.Tensor
+    b: synth.Tensor | None
+    gy: synth.Tensor
+    extra: dict = field(default_factory=dict)
+
+
+def make_inputs(L: Layer, seed: int = 0, branch: int = 0, gy_channels: int | None = None) -> Inputs:
+    """x, w, bias and grad_out for one layer, drawn as the module docstring says."""
+    xs = (L.N, L.C, L.H, L.W)
+    if L.x_dist == "uniform":
+        x = synth.uniform_tensor(xs, L.dtype, seed, synth.STREAM_X)
+    else:
+        x = synth.normal_tensor(xs, L.dtype, seed, synth.STREAM_X)
+    w_std = L.w_std if L.w_std is not None else 1.0 / L.k
+    w = synth.normal_tensor((L.OC, L.k, L.k), L.dtype, seed, synth.STREAM_W + 16 * branch, std=w_std)
+    b = (synth.normal_tensor((L.OC,), L.dtype, seed, synth.STREAM_B + 16 * branch, std=L.b_std)
+         if L.bias else None)
+    gc = L.OC if gy_channels is None else gy_channels
+    gy = synth.normal_tensor((L.N, gc, L.Ho, L.Wo), L.dtype, seed, synth.STREAM_GY)
+    return Inputs(x, w, b, gy)

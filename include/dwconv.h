@@ -1,0 +1,162 @@
+/*
+ * libdwconv -- depthwise 2-D convolution on NVIDIA GB300 (sm_103a).
+ *
+ * C ABI. Every entry point takes a descriptor, plain pointers and sizes, and
+ * a CUDA stream. No framework types cross this boundary.
+ *
+ * The operation (sources: "Spatial Depthwise Convolution on the GPU #3057",
+ * the forward binding conv_depthwise2d_forward_out(output, input, weight,
+ * kernel_size, bias, stride, padding, dilation) and the commits that add
+ * padding, strides, dilation, the depth multiplier, bias and grad_bias; the
+ * MegEngine large-kernel depthwise article, "From convolution to matrix
+ * multiplication", for the per-channel sliding window; the
+ * DynamicConvolutionOperator README, "Solution", for branches stored straight
+ * into strided slices of one concatenated output):
+ *
+ *   x  : [N, C, H, W]                 input, NCHW, contiguous
+ *   w  : [C*m, kh, kw]                filters (PyTorch's [C*m, 1, kh, kw])
+ *   b  : [C*m]                        bias, optional
+ *   y  : [N, out_c_total, Ho, Wo]     output; this call owns channels
+ *                                     [out_c_offset, out_c_offset + C*m)
+ *   Ho = floor((H + 2*pad_h - dil_h*(kh-1) - 1) / stride_h) + 1   (same for Wo)
+ *
+ *   y[n, off + c*m + j, oh, ow] = b[c*m + j]
+ *       + sum_{a<kh, b<kw} w[c*m + j, a, b] * x[n, c, oh*sh - ph + a*dh, ow*sw - pw + b*dw]
+ *
+ * Taps outside the input read zero (zero padding). This is cross-correlation
+ * (no kernel flip), the convention of PyTorch's conv2d. Output channel
+ * oc = c*m + j reads input channel c (PyTorch groups = C).
+ *
+ * Conventions for every entry point:
+ *  - Ownership: the caller owns all memory, including the bwd_weight
+ *    workspace. The library never allocates, frees or synchronises, and
+ *    never changes the current device. Data pointers are device pointers on
+ *    the current device (or managed memory).
+ *  - Precision: x, w, b, y, gy, gx, gw, gb all share desc->dtype. Arithmetic
+ *    is fp32 (fp16 / bf16 operands are widened exactly, products and sums are
+ *    fp32); results are rounded to the storage type once, round to nearest even.
+ *  - Work is enqueued on `stream` (0 = legacy default stream) and nothing
+ *    waits for it. A launch failure returns DWCONV_ERR_CUDA; faults during
+ *    execution surface at the caller's next synchronisation.
+ *  - Errors: arguments are checked on the host before any launch; on any
+ *    error nothing is enqueued and nothing is written. Nothing prints or aborts.
+ *  - Alignment: each pointer must be aligned to its element size
+ *    (DWCONV_ERR_MISALIGNED otherwise); wider alignment is used when present.
+ *  - Determinism: every entry point gives bitwise identical results on
+ *    repeated calls with the same inputs on the same GPU.
+ *  - Thread safety: no mutable global state; calls may come from any thread.
+ *  - Empty batch (N == 0) is valid and enqueues nothing.
+ */
+#ifndef DWCONV_H_
+#define DWCONV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DWCONV_F32 = 0,
+  DWCONV_F16 = 1,
+  DWCONV_BF16 = 2
+} dwconv_dtype_t;
+
+typedef enum {
+  DWCONV_OK = 0,
+  DWCONV_ERR_INVALID_ARG = 1,   /* null pointer, bad size, Ho or Wo < 1, slice out of range */
+  DWCONV_ERR_UNSUPPORTED = 2,   /* unknown dtype, kernel larger than 255, ... */
+  DWCONV_ERR_MISALIGNED = 3,    /* pointer not aligned to its element size */
+  DWCONV_ERR_WORKSPACE = 4,     /* bwd_weight workspace missing or too small */
+  DWCONV_ERR_CUDA = 5           /* a CUDA runtime call or launch failed */
+} dwconv_status_t;
+
+/* One depthwise convolution. 88 bytes, no padding holes. */
+typedef struct {
+  int64_t N, C, H, W;          /* input NCHW; N >= 0, C, H, W >= 1 */
+  int32_t multiplier;          /* m >= 1: output channel c*m + j reads input channel c */
+  int32_t kh, kw;              /* 1 .. 255 */
+  int32_t stride_h, stride_w;  /* >= 1 */
+  int32_t pad_h, pad_w;        /* >= 0, zero padding on both sides */
+  int32_t dil_h, dil_w;        /* >= 1 */
+  int32_t dtype;               /* dwconv_dtype_t */
+  int64_t out_c_offset;        /* first channel of this op's slice in y / gy (>= 0) */
+  int64_t out_c_total;         /* channel count of the y / gy buffer; 0 means C*m */
+} dwconv2d_desc_t;
+
+/* Output spatial size. Returns DWCONV_ERR_INVALID_ARG if the descriptor is
+ * invalid (Ho or Wo would be < 1, slice out of range, ...). */
+dwconv_status_t dwconv2d_output_shape(const dwconv2d_desc_t* desc, int64_t* Ho, int64_t* Wo);
+
+/* Forward (#3057 forward kernel; the bias of its "add bias for forward"
+ * commit). Writes only channels [off, off + C*m) of y; the other channels of
+ * y are left bit-identical. bias may be NULL. */
+dwconv_status_t dwconv2d_fwd(const dwconv2d_desc_t* desc, const void* x, const void* w,
+                             const void* bias, void* y, cudaStream_t stream);
+
+/* Gradient with respect to the input (#3057 grad-input kernel): the adjoint
+ * of dwconv2d_fwd in x,
+ *   gx[n, c, ih, iw] = sum_j sum_{a, b} w[c*m+j, a, b] * gy[n, off+c*m+j, oh, ow]
+ * over the (oh, ow, a, b) with oh*sh - ph + a*dh == ih and
+ * ow*sw - pw + b*dw == iw. gy is read from the same channel slice that the
+ * forward wrote. accumulate = 0 overwrites gx, 1 adds to it (gx += ...). */
+dwconv_status_t dwconv2d_bwd_data(const dwconv2d_desc_t* desc, const void* gy, const void* w,
+                                  void* gx, int accumulate, cudaStream_t stream);
+
+/* Bytes of device workspace dwconv2d_bwd_weight needs for this descriptor
+ * (0 if the descriptor is invalid). Depends only on the descriptor. */
+size_t dwconv2d_bwd_weight_workspace_size(const dwconv2d_desc_t* desc);
+
+/* Gradients with respect to the filters and bias (#3057 grad-weight kernel,
+ * extended there to padding, stride and dilation; grad_bias from its
+ * output_mask):
+ *   gw[oc, a, b] = sum_{n, oh, ow} gy[n, off+oc, oh, ow] * x[n, oc/m, oh*sh-ph+a*dh, ow*sw-pw+b*dw]
+ *   gb[oc]       = sum_{n, oh, ow} gy[n, off+oc, oh, ow]
+ * gw and gbias are overwritten; either may be NULL (then it is not computed).
+ * Two launches: per-chunk fp32 partial sums into `workspace`, then a sum of
+ * the chunks in index order, so the result is bitwise reproducible.
+ * workspace_bytes must be >= dwconv2d_bwd_weight_workspace_size(desc); the
+ * workspace must be 16-byte aligned and must not be used concurrently. */
+dwconv_status_t dwconv2d_bwd_weight(const dwconv2d_desc_t* desc, const void* x, const void* gy,
+                                    void* gw, void* gbias, void* workspace,
+                                    size_t workspace_bytes, cudaStream_t stream);
+
+/* Fused multi-branch forward (the DynamicConvolutionOperator's single launch
+ * for dilation 1, 3, 5 whose results are stored straight into slices of one
+ * concatenated tensor): nbranch (1..8) descriptors over the same x. All
+ * branches must share N, C, H, W, multiplier, dtype and out_c_total, and give
+ * equal Ho, Wo; each has its own kernel size, stride, padding, dilation and
+ * out_c_offset. Slices must not overlap. w[i] and bias[i] (bias or bias[i]
+ * may be NULL) belong to branch i. One launch reads each x tile once. */
+dwconv_status_t dwconv2d_fwd_multi(int nbranch, const dwconv2d_desc_t* descs, const void* x,
+                                   const void* const* w, const void* const* bias, void* y,
+                                   cudaStream_t stream);
+
+/* Input gradient of dwconv2d_fwd_multi: gx = sum over branches of each
+ * branch's dwconv2d_bwd_data (the chain rule through the concatenation),
+ * computed in one launch and written once (gx is overwritten). */
+dwconv_status_t dwconv2d_bwd_data_multi(int nbranch, const dwconv2d_desc_t* descs, const void* gy,
+                                        const void* const* w, void* gx, cudaStream_t stream);
+
+/* Static text for a status code. */
+const char* dwconv_status_string(dwconv_status_t status);
+
+/* Name of the kernel family the planner picks for a pass (0 = fwd,
+ * 1 = bwd_data, 2 = bwd_weight) of this descriptor, or "invalid". Host only;
+ * for logs and tests. */
+const char* dwconv2d_plan_name(const dwconv2d_desc_t* desc, int pass);
+
+/* Measurement helper, not part of the convolution: runs a register-only
+ * fp32 FMA loop on every SM (`blocks` x 256 threads, `iters` iterations of 16
+ * independent FMA chains) and writes one float per thread to `sink`
+ * (blocks * 256 floats) so the work cannot be elided. Time it with events to
+ * get the device's fp32 FMA rate: 2 * 16 * iters * blocks * 256 FLOP. */
+dwconv_status_t dwconv_fma_probe(int blocks, int iters, float* sink, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DWCONV_H_ */

@@ -1,0 +1,144 @@
+"""The C-ABI library on the host: it builds, loads, exports every symbol the
+header declares, and rejects bad arguments before any launch (no GPU needed:
+each call below fails validation, so nothing is enqueued)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from depthwise_convolution_dwconv2d_gb300 import binding as B
+from depthwise_convolution_dwconv2d_gb300 import build as BLD
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dwconv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    BLD.build()
+    return B.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(dwconv\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_and_binding_agree():
+    assert declared_functions() == sorted(B.SYMBOLS)
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = os.popen(f"nm -D --defined-only {B.lib_path()}").read()
+    for name in declared_functions():
+        assert re.search(rf"\bT {name}\b", out), f"{name} not exported"
+
+
+def test_desc_layout():
+    assert ctypes.sizeof(B.Desc) == 88
+    assert B.Desc.out_c_offset.offset == 72 and B.Desc.dtype.offset == 68
+
+
+def test_output_shape(lib):
+    assert B.dwconv2d_output_shape(B.make_desc(64, 128, 56, 56, 3, 1, 1)) == (56, 56)
+    assert B.dwconv2d_output_shape(B.make_desc(64, 64, 112, 112, 3, 2, 1)) == (56, 56)
+    assert B.dwconv2d_output_shape(B.make_desc(64, 1024, 7, 7, 3, 2, 1)) == (4, 4)
+    assert B.dwconv2d_output_shape(B.make_desc(2, 64, 256, 256, 3, 1, 5, 5)) == (256, 256)
+    assert B.dwconv2d_output_shape(B.make_desc(1, 1, 5, 5, 2, 2, 0, 2)) == (2, 2)
+    assert B.dwconv2d_output_shape(B.make_desc(1, 1, 3, 7, (5, 3), (1, 2), (1, 0))) == (1, 3)
+
+
+def status_of(fn, *args):
+    try:
+        fn(*args)
+    except B.DwconvError as e:
+        return e.status
+    return 0
+
+
+INVALID, UNSUPPORTED, MISALIGNED, WORKSPACE = 1, 2, 3, 4
+P = 0x10000  # a well-aligned fake address: validation fails before any use
+
+
+@pytest.mark.parametrize("desc,want", [
+    (B.make_desc(1, 0, 8, 8), INVALID),                 # C < 1
+    (B.make_desc(-1, 3, 8, 8), INVALID),                # N < 0
+    (B.make_desc(1, 3, 0, 8), INVALID),                 # H < 1
+    (B.make_desc(1, 3, 8, 8, 0), INVALID),              # kernel < 1
+    (B.make_desc(1, 3, 8, 8, 3, 0), INVALID),           # stride < 1
+    (B.make_desc(1, 3, 8, 8, 3, 1, -1), INVALID),       # pad < 0
+    (B.make_desc(1, 3, 8, 8, 3, 1, 1, 0), INVALID),     # dilation < 1
+    (B.make_desc(1, 3, 2, 2, 5, 1, 0), INVALID),        # Ho < 1
+    (B.make_desc(1, 3, 8, 8, multiplier=0), INVALID),
+    (B.make_desc(1, 3, 8, 8, out_c_offset=2, out_c_total=4), INVALID),   # slice overflows
+    (B.make_desc(1, 3, 8, 8, out_c_offset=-1, out_c_total=9), INVALID),
+    (B.make_desc(1, 3, 8, 8, dtype=7), UNSUPPORTED),
+    (B.make_desc(1, 3, 300, 300, 256, 1, 128), UNSUPPORTED),  # kernel > 255
+])
+def test_bad_descriptors_rejected(lib, desc, want):
+    assert status_of(B.dwconv2d_fwd, desc, P, P, None, P, 0) == want
+    assert status_of(B.dwconv2d_bwd_data, desc, P, P, P, 0, 0) == want
+    assert status_of(B.dwconv2d_bwd_weight, desc, P, P, P, None, P, 1 << 30, 0) == want
+    assert B.dwconv2d_bwd_weight_workspace_size(desc) == 0
+    assert B.dwconv2d_plan_name(desc, 0) == "invalid"
+
+
+def test_null_and_misaligned_pointers(lib):
+    d = B.make_desc(2, 3, 8, 8, 3, 1, 1)
+    assert status_of(B.dwconv2d_fwd, d, None, P, None, P, 0) == INVALID
+    assert status_of(B.dwconv2d_fwd, d, P, None, None, P, 0) == INVALID
+    assert status_of(B.dwconv2d_fwd, d, P, P, None, None, 0) == INVALID
+    assert status_of(B.dwconv2d_fwd, d, P + 2, P, None, P, 0) == MISALIGNED
+    assert status_of(B.dwconv2d_fwd, d, P, P, P + 1, P, 0) == MISALIGNED
+    h = B.make_desc(2, 3, 8, 8, 3, 1, 1, dtype="bf16")
+    assert status_of(B.dwconv2d_fwd, h, P + 1, P, None, P, 0) == MISALIGNED
+    assert status_of(B.dwconv2d_bwd_data, d, P, P, P, 2, 0) == INVALID   # accumulate not 0/1
+    assert status_of(B.dwconv2d_bwd_data, d, P, P, P + 2, 0, 0) == MISALIGNED
+
+
+def test_workspace_checks(lib):
+    d = B.make_desc(4, 8, 16, 16, 3, 1, 1)
+    need = B.dwconv2d_bwd_weight_workspace_size(d)
+    assert need > 0 and need % 256 == 0
+    assert status_of(B.dwconv2d_bwd_weight, d, P, P, P, None, None, need, 0) == WORKSPACE
+    assert status_of(B.dwconv2d_bwd_weight, d, P, P, P, None, P, need - 1, 0) == WORKSPACE
+    assert status_of(B.dwconv2d_bwd_weight, d, P, P, P, None, P + 8, need, 0) == MISALIGNED
+    # nothing requested: a valid no-op that touches nothing
+    assert status_of(B.dwconv2d_bwd_weight, d, None, None, None, None, None, 0, 0) == 0
+
+
+def test_empty_batch_is_noop(lib):
+    d = B.make_desc(0, 3, 8, 8, 3, 1, 1)
+    assert status_of(B.dwconv2d_fwd, d, None, P, None, None, 0) == 0
+    assert status_of(B.dwconv2d_bwd_data, d, None, P, None, 0, 0) == 0
+
+
+def test_multi_branch_validation(lib):
+    mk = lambda d, off: B.make_desc(2, 4, 16, 16, 3, 1, d, d, out_c_offset=off, out_c_total=12)
+    ok = [mk(1, 0), mk(3, 4), mk(5, 8)]
+    # unequal output size
+    bad_size = [mk(1, 0), B.make_desc(2, 4, 16, 16, 3, 1, 0, 1, out_c_offset=4, out_c_total=12)]
+    assert status_of(B.dwconv2d_fwd_multi, bad_size, P, [P, P], None, P, 0) == INVALID
+    # overlapping slices
+    assert status_of(B.dwconv2d_fwd_multi, [mk(1, 0), mk(3, 2)], P, [P, P], None, P, 0) == INVALID
+    # too many branches / none
+    assert status_of(B.dwconv2d_fwd_multi, ok * 3, P, [P] * 9, None, P, 0) == INVALID
+    assert status_of(B.dwconv2d_bwd_data_multi, [], P, [], P, 0) == INVALID
+    # differing c_total
+    odd = [mk(1, 0), B.make_desc(2, 4, 16, 16, 3, 1, 3, 3, out_c_offset=4, out_c_total=13)]
+    assert status_of(B.dwconv2d_bwd_data_multi, odd, P, [P, P], P, 0) == INVALID
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert B.dwconv_status_string(s)
+    assert B.dwconv_status_string(99) == "unknown status"
+
+
+def test_plan_names(lib):
+    assert B.dwconv2d_plan_name(B.make_desc(64, 128, 56, 56, 3, 1, 1), 0) in ("generic", "tile", "large")
+    assert B.dwconv2d_plan_name(B.make_desc(64, 128, 56, 56, 3, 1, 1), 3) == "invalid"
