@@ -304,10 +304,10 @@ def gpu_arm(args, rank, world):
             wdev = [dd for dd, _ in wd]
             cl = layer_calls(item)
             nb = len(brs)
-            fused = B.dwconv2d_plan_name(descs[0], 0) != "generic"
+            fused = B.dwconv2d_multi_plan_name(descs) == "tile"
             calls.append(("fwd", item.label(), cl[0][1], cl[0][2], 1 if fused else nb,
                           lambda descs=descs, x=x, wdev=wdev, y=y: B.dwconv2d_fwd_multi(descs, x, wdev, None, y, stream)))
-            calls.append(("bwd_data", item.label(), cl[1][1], cl[1][2], 1 if fused else nb,
+            calls.append(("bwd_data", item.label(), cl[1][1], cl[1][2], 1,
                           lambda descs=descs, gy=gy, wdev=wdev, gx=gx: B.dwconv2d_bwd_data_multi(descs, gy, wdev, gx, stream)))
             for i, dd in enumerate(descs):
                 calls.append(("bwd_weight", f"{item.label()}_br{i}", cl[2 + i][1], cl[2 + i][2], 2,

@@ -23,7 +23,7 @@ STATUS = {0: "DWCONV_OK", 1: "DWCONV_ERR_INVALID_ARG", 2: "DWCONV_ERR_UNSUPPORTE
 SYMBOLS = ("dwconv2d_output_shape", "dwconv2d_fwd", "dwconv2d_bwd_data",
            "dwconv2d_bwd_weight_workspace_size", "dwconv2d_bwd_weight", "dwconv2d_fwd_multi",
            "dwconv2d_bwd_data_multi", "dwconv_status_string", "dwconv2d_plan_name",
-           "dwconv_fma_probe")
+           "dwconv2d_multi_plan_name", "dwconv_fma_probe")
 
 
 class DwconvError(RuntimeError):
@@ -91,9 +91,12 @@ def load():
     lib.dwconv_status_string.restype = ctypes.c_char_p
     lib.dwconv2d_plan_name.argtypes = [P, ctypes.c_int]
     lib.dwconv2d_plan_name.restype = ctypes.c_char_p
+    lib.dwconv2d_multi_plan_name.argtypes = [ctypes.c_int, P]
+    lib.dwconv2d_multi_plan_name.restype = ctypes.c_char_p
     lib.dwconv_fma_probe.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp]
     for name in SYMBOLS:
-        if name not in ("dwconv2d_bwd_weight_workspace_size", "dwconv_status_string", "dwconv2d_plan_name"):
+        if name not in ("dwconv2d_bwd_weight_workspace_size", "dwconv_status_string", "dwconv2d_plan_name",
+                        "dwconv2d_multi_plan_name"):
             getattr(lib, name).restype = st
     _lib = lib
     return lib
@@ -181,6 +184,10 @@ def dwconv_status_string(status: int) -> str:
 
 def dwconv2d_plan_name(desc: Desc, pass_: int) -> str:
     return load().dwconv2d_plan_name(ctypes.byref(desc), int(pass_)).decode()
+
+
+def dwconv2d_multi_plan_name(descs) -> str:
+    return load().dwconv2d_multi_plan_name(len(descs), _desc_array(descs)).decode()
 
 
 def dwconv_fma_probe(blocks: int, iters: int, sink, stream=None):

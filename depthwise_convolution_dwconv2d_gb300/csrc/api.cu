@@ -134,6 +134,12 @@ const char* dwconv2d_plan_name(const dwconv2d_desc_t* desc, int pass) {
   return algo_name(pass == 0 ? plan_fwd(c) : pass == 1 ? plan_bwd_data(c) : plan_bwd_weight(c).algo);
 }
 
+const char* dwconv2d_multi_plan_name(int nbranch, const dwconv2d_desc_t* descs) {
+  Conv cs[kMaxBranches];
+  if (make_multi(nbranch, descs, cs) != DWCONV_OK) return "invalid";
+  return algo_name(plan_multi(nbranch, cs));
+}
+
 dwconv_status_t dwconv2d_fwd(const dwconv2d_desc_t* desc, const void* x, const void* w,
                              const void* bias, void* y, cudaStream_t stream) {
   Conv c;

@@ -71,6 +71,12 @@ cudaError_t fwd_generic(const Conv& c, const void* x, const void* w, const void*
                         cudaStream_t s);
 cudaError_t bwd_data_generic(const Conv& c, const void* gy, const void* w, void* gx,
                              bool accumulate, cudaStream_t s);
+struct MultiGeneric {
+  int nb;
+  Conv c[8];
+  const void* w[8];
+};
+cudaError_t bwd_data_multi_generic(const MultiGeneric& m, const void* gy, void* gx, cudaStream_t s);
 // pass 1 writes ws[chunk][oc][taps + 1] (last slot = bias) for `chunks` batch chunks.
 cudaError_t bwd_weight_generic_pass1(const Conv& c, const void* x, const void* gy, float* ws,
                                      int chunks, bool want_w, bool want_b, cudaStream_t s);

@@ -149,6 +149,47 @@ bwd_weight_pass2_kernel(Conv c, const float* __restrict__ ws, int chunks, T* gw,
   }
 }
 
+// Sum over branches of each branch's grad-input, accumulated in fp32 and
+// rounded once (the chain rule through a channel concatenation).
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+bwd_data_multi_generic_kernel(MultiGeneric g, const T* __restrict__ gy, T* gx) {
+  const Conv& c0 = g.c[0];
+  const int64_t total = c0.N * c0.C * c0.H * c0.W;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    int64_t t = idx;
+    const int64_t iw = t % c0.W; t /= c0.W;
+    const int64_t ih = t % c0.H; t /= c0.H;
+    const int64_t ch = t % c0.C;
+    const int64_t n = t / c0.C;
+    float acc = 0.f;
+    for (int br = 0; br < g.nb; ++br) {
+      const Conv& c = g.c[br];
+      const T* w = (const T*)g.w[br];
+      for (int j = 0; j < c.m; ++j) {
+        const int64_t oc = ch * c.m + j;
+        const T* gp = gy + c.y_base(n, oc);
+        const T* wp = w + oc * c.kh * c.kw;
+        for (int a = 0; a < c.kh; ++a) {
+          const int64_t nh = ih + c.ph - (int64_t)a * c.dh;
+          if (nh < 0 || nh % c.sh != 0) continue;
+          const int64_t oh = nh / c.sh;
+          if (oh >= c.Ho) continue;
+          for (int bb = 0; bb < c.kw; ++bb) {
+            const int64_t nw = iw + c.pw - (int64_t)bb * c.dw;
+            if (nw < 0 || nw % c.sw != 0) continue;
+            const int64_t ow = nw / c.sw;
+            if (ow >= c.Wo) continue;
+            acc = fmaf(ld(wp + a * c.kw + bb), ld(gp + oh * c.Wo + ow), acc);
+          }
+        }
+      }
+    }
+    gx[idx] = from_f<T>(acc);
+  }
+}
+
 int grid_for(int64_t total) {
   int64_t g = (total + kThreads - 1) / kThreads;
   const int64_t cap = 152 * 32;  // enough resident blocks to fill every SM
@@ -171,6 +212,14 @@ cudaError_t bwd_data_generic(const Conv& c, const void* gy, const void* w, void*
   const int g = grid_for(c.N * c.C * c.H * c.W);
   DWCONV_DISPATCH_DTYPE(c.dtype, T,
     bwd_data_generic_kernel<T><<<g, kThreads, 0, s>>>(c, (const T*)gy, (const T*)w, (T*)gx, accumulate));
+  return cudaGetLastError();
+}
+
+cudaError_t bwd_data_multi_generic(const MultiGeneric& m, const void* gy, void* gx, cudaStream_t s) {
+  const Conv& c = m.c[0];
+  const int g = grid_for(c.N * c.C * c.H * c.W);
+  DWCONV_DISPATCH_DTYPE(c.dtype, T,
+    bwd_data_multi_generic_kernel<T><<<g, kThreads, 0, s>>>(m, (const T*)gy, (T*)gx));
   return cudaGetLastError();
 }
 

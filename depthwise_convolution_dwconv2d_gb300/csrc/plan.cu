@@ -28,15 +28,18 @@ const char* algo_name(Algo a) {
 
 Algo plan_fwd(const Conv& c) {
   if (force_generic()) return Algo::Generic;
+  if (tile::fwd_supported(c)) return Algo::Tile;
   return Algo::Generic;
 }
 
 Algo plan_bwd_data(const Conv& c) {
   if (force_generic()) return Algo::Generic;
+  if (c.sh == 1 ? tile::bwd1_supported(c) : tile::bwd2_supported(c)) return Algo::Tile;
   return Algo::Generic;
 }
 
 WPlan plan_bwd_weight(const Conv& c) {
+  if (!force_generic() && tile::wgrad_supported(c)) return WPlan{Algo::Tile, tile::wgrad_chunks(c)};
   // generic first pass: a chunk of whole samples per block, at most 2^20
   // positions per chunk so each thread's serial chain stays <= 4096 terms.
   const int64_t hw = c.Ho * c.Wo;
@@ -51,6 +54,7 @@ WPlan plan_bwd_weight(const Conv& c) {
 cudaError_t run_fwd(Algo a, const Conv& c, const void* x, const void* w, const void* b, void* y,
                     cudaStream_t s) {
   switch (a) {
+    case Algo::Tile: return tile::fwd(c, x, w, b, y, s);
     default: return fwd_generic(c, x, w, b, y, s);
   }
 }
@@ -58,6 +62,8 @@ cudaError_t run_fwd(Algo a, const Conv& c, const void* x, const void* w, const v
 cudaError_t run_bwd_data(Algo a, const Conv& c, const void* gy, const void* w, void* gx,
                          bool accumulate, cudaStream_t s) {
   switch (a) {
+    case Algo::Tile:
+      return c.sh == 1 ? tile::bwd1(c, gy, w, gx, accumulate, s) : tile::bwd2(c, gy, w, gx, accumulate, s);
     default: return bwd_data_generic(c, gy, w, gx, accumulate, s);
   }
 }
@@ -66,6 +72,9 @@ cudaError_t run_bwd_weight(const WPlan& p, const Conv& c, const void* x, const v
                            void* gb, float* ws, cudaStream_t s) {
   cudaError_t e;
   switch (p.algo) {
+    case Algo::Tile:
+      e = tile::wgrad(c, x, gy, ws, p.chunks, s);
+      break;
     default:
       e = bwd_weight_generic_pass1(c, x, gy, ws, p.chunks, gw != nullptr, gb != nullptr, s);
       break;
@@ -74,8 +83,15 @@ cudaError_t run_bwd_weight(const WPlan& p, const Conv& c, const void* x, const v
   return bwd_weight_pass2(c, ws, p.chunks, gw, gb, s);
 }
 
+Algo plan_multi(int nb, const Conv* cs) {
+  if (!force_generic() && tile::multi_supported(nb, cs)) return Algo::Tile;
+  return Algo::Generic;
+}
+
 cudaError_t run_fwd_multi(int nb, const Conv* cs, const void* x, const void* const* w,
                           const void* const* bias, void* y, cudaStream_t s) {
+  if (plan_multi(nb, cs) == Algo::Tile) return tile::fwd_multi(nb, cs, x, w, bias, y, s);
+  // branches write disjoint slices: one launch per branch
   for (int i = 0; i < nb; ++i) {
     cudaError_t e = run_fwd(plan_fwd(cs[i]), cs[i], x, w[i], bias ? bias[i] : nullptr, y, s);
     if (e != cudaSuccess) return e;
@@ -85,11 +101,14 @@ cudaError_t run_fwd_multi(int nb, const Conv* cs, const void* x, const void* con
 
 cudaError_t run_bwd_data_multi(int nb, const Conv* cs, const void* gy, const void* const* w,
                                void* gx, cudaStream_t s) {
+  if (plan_multi(nb, cs) == Algo::Tile) return tile::bwd_multi(nb, cs, gy, w, gx, s);
+  MultiGeneric m{};
+  m.nb = nb;
   for (int i = 0; i < nb; ++i) {
-    cudaError_t e = run_bwd_data(plan_bwd_data(cs[i]), cs[i], gy, w[i], gx, i > 0, s);
-    if (e != cudaSuccess) return e;
+    m.c[i] = cs[i];
+    m.w[i] = w[i];
   }
-  return cudaSuccess;
+  return bwd_data_multi_generic(m, gy, gx, s);
 }
 
 }  // namespace dwconv

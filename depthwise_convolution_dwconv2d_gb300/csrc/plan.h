@@ -34,4 +34,27 @@ cudaError_t run_fwd_multi(int nb, const Conv* cs, const void* x, const void* con
 cudaError_t run_bwd_data_multi(int nb, const Conv* cs, const void* gy, const void* const* w,
                                void* gx, cudaStream_t s);
 
+namespace tile {
+// tile_fwd.cu
+bool fwd_supported(const Conv& c);
+cudaError_t fwd(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s);
+bool bwd1_supported(const Conv& c);
+cudaError_t bwd1(const Conv& c, const void* gy, const void* w, void* gx, bool acc, cudaStream_t s);
+// tile_bwd2.cu
+bool bwd2_supported(const Conv& c);
+cudaError_t bwd2(const Conv& c, const void* gy, const void* w, void* gx, bool acc, cudaStream_t s);
+// tile_wgrad.cu (first pass; the second pass is bwd_weight_pass2)
+bool wgrad_supported(const Conv& c);
+int wgrad_chunks(const Conv& c);
+cudaError_t wgrad(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s);
+// tile_multi.cu
+bool multi_supported(int nb, const Conv* cs);
+cudaError_t fwd_multi(int nb, const Conv* cs, const void* x, const void* const* w,
+                      const void* const* bias, void* y, cudaStream_t s);
+cudaError_t bwd_multi(int nb, const Conv* cs, const void* gy, const void* const* w, void* gx,
+                      cudaStream_t s);
+}  // namespace tile
+
+Algo plan_multi(int nb, const Conv* cs);
+
 }  // namespace dwconv

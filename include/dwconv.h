@@ -129,14 +129,17 @@ dwconv_status_t dwconv2d_bwd_weight(const dwconv2d_desc_t* desc, const void* x, 
  * branches must share N, C, H, W, multiplier, dtype and out_c_total, and give
  * equal Ho, Wo; each has its own kernel size, stride, padding, dilation and
  * out_c_offset. Slices must not overlap. w[i] and bias[i] (bias or bias[i]
- * may be NULL) belong to branch i. One launch reads each x tile once. */
+ * may be NULL) belong to branch i. For 2 or 3 branches of 3x3 filters at
+ * stride 1, m = 1 and dilation sets {1,3,5}, {1,2,3}, {1,2}, {1,3} one launch
+ * reads each x tile once and writes every branch; other sets run one launch
+ * per branch (see dwconv2d_multi_plan_name). */
 dwconv_status_t dwconv2d_fwd_multi(int nbranch, const dwconv2d_desc_t* descs, const void* x,
                                    const void* const* w, const void* const* bias, void* y,
                                    cudaStream_t stream);
 
 /* Input gradient of dwconv2d_fwd_multi: gx = sum over branches of each
  * branch's dwconv2d_bwd_data (the chain rule through the concatenation),
- * computed in one launch and written once (gx is overwritten). */
+ * accumulated in fp32 in one launch and rounded once (gx is overwritten). */
 dwconv_status_t dwconv2d_bwd_data_multi(int nbranch, const dwconv2d_desc_t* descs, const void* gy,
                                         const void* const* w, void* gx, cudaStream_t stream);
 
@@ -147,6 +150,12 @@ const char* dwconv_status_string(dwconv_status_t status);
  * 1 = bwd_data, 2 = bwd_weight) of this descriptor, or "invalid". Host only;
  * for logs and tests. */
 const char* dwconv2d_plan_name(const dwconv2d_desc_t* desc, int pass);
+
+/* Kernel family used by dwconv2d_fwd_multi / dwconv2d_bwd_data_multi for
+ * these branches ("tile" = the fused single-launch kernels, "generic" = the
+ * any-shape fallback: one launch per branch for the forward, one launch for
+ * the grad-input), or "invalid". Host only. */
+const char* dwconv2d_multi_plan_name(int nbranch, const dwconv2d_desc_t* descs);
 
 /* Measurement helper, not part of the convolution: runs a register-only
  * fp32 FMA loop on every SM (`blocks` x 256 threads, `iters` iterations of 16
