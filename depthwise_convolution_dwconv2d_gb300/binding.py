@@ -23,7 +23,7 @@ STATUS = {0: "DWCONV_OK", 1: "DWCONV_ERR_INVALID_ARG", 2: "DWCONV_ERR_UNSUPPORTE
 SYMBOLS = ("dwconv2d_output_shape", "dwconv2d_fwd", "dwconv2d_bwd_data",
            "dwconv2d_bwd_weight_workspace_size", "dwconv2d_bwd_weight", "dwconv2d_fwd_multi",
            "dwconv2d_bwd_data_multi", "dwconv_status_string", "dwconv2d_plan_name",
-           "dwconv2d_multi_plan_name", "dwconv_fma_probe")
+           "dwconv2d_multi_plan_name", "dwconv_fma_probe", "dwconv2d_bwd_weight_noalloc")
 
 
 class DwconvError(RuntimeError):
@@ -85,6 +85,7 @@ def load():
     lib.dwconv2d_bwd_weight_workspace_size.argtypes = [P]
     lib.dwconv2d_bwd_weight_workspace_size.restype = ctypes.c_size_t
     lib.dwconv2d_bwd_weight.argtypes = [P, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    lib.dwconv2d_bwd_weight_noalloc.argtypes = [P, vp, vp, vp, vp, vp]
     lib.dwconv2d_fwd_multi.argtypes = [ctypes.c_int, P, vp, ctypes.POINTER(vp), ctypes.POINTER(vp), vp, vp]
     lib.dwconv2d_bwd_data_multi.argtypes = [ctypes.c_int, P, vp, ctypes.POINTER(vp), vp, vp]
     lib.dwconv_status_string.argtypes = [st]
@@ -155,6 +156,15 @@ def dwconv2d_bwd_weight(desc: Desc, x, gy, gw, gbias, workspace, workspace_bytes
     _check(load().dwconv2d_bwd_weight(ctypes.byref(desc), _ptr(x), _ptr(gy), _ptr(gw), _ptr(gbias),
                                       _ptr(workspace), int(workspace_bytes), _stream(stream)),
            "dwconv2d_bwd_weight")
+
+
+def dwconv2d_bwd_weight_noalloc(desc: Desc, x, gy, gw, gbias, stream=None):
+    """dwconv2d_bwd_weight for callers that cannot allocate device memory:
+    the partial sums use the library's fixed 8 MiB device array instead of a
+    workspace argument (see include/dwconv.h)."""
+    _check(load().dwconv2d_bwd_weight_noalloc(ctypes.byref(desc), _ptr(x), _ptr(gy), _ptr(gw),
+                                              _ptr(gbias), _stream(stream)),
+           "dwconv2d_bwd_weight_noalloc")
 
 
 def _desc_array(descs):

@@ -44,7 +44,9 @@
  *    (DWCONV_ERR_MISALIGNED otherwise); wider alignment is used when present.
  *  - Determinism: every entry point gives bitwise identical results on
  *    repeated calls with the same inputs on the same GPU.
- *  - Thread safety: no mutable global state; calls may come from any thread.
+ *  - Thread safety: no mutable global state (apart from the per-device
+ *    address that dwconv2d_bwd_weight_noalloc caches); calls may come from
+ *    any thread.
  *  - Empty batch (N == 0) is valid and enqueues nothing.
  */
 #ifndef DWCONV_H_
@@ -122,6 +124,29 @@ size_t dwconv2d_bwd_weight_workspace_size(const dwconv2d_desc_t* desc);
 dwconv_status_t dwconv2d_bwd_weight(const dwconv2d_desc_t* desc, const void* x, const void* gy,
                                     void* gw, void* gbias, void* workspace,
                                     size_t workspace_bytes, cudaStream_t stream);
+
+/* Weight and bias gradients without a caller-provided workspace.
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory when they need the gradient -- for
+ * example code inside a host application that owns every device allocation
+ * through its own pool, or a latency-critical loop where a cudaMalloc (which
+ * may synchronise the device) is not acceptable.
+ * Same arguments, results and errors as dwconv2d_bwd_weight minus the
+ * workspace: the partial sums go to a fixed 8 MiB (8388608-byte) array that
+ * is part of the library's device code, so every GPU that loads the library
+ * holds those 8 MiB until the process exits. Descriptors whose
+ * dwconv2d_bwd_weight_workspace_size exceeds 8 MiB are rejected with
+ * DWCONV_ERR_WORKSPACE and nothing is enqueued. The call allocates and frees
+ * nothing. The first call on each device (with that device current) looks up
+ * the array's device address and keeps it for later calls; make that first
+ * call before any stream capture. All calls share the one array and each
+ * call's first pass overwrites every slot its second pass reads, so stale
+ * contents from an earlier call do no harm -- but calls that may run at the
+ * same time on the GPU (different streams, or different host threads) race
+ * on the array and must be serialised by the caller. */
+dwconv_status_t dwconv2d_bwd_weight_noalloc(const dwconv2d_desc_t* desc, const void* x,
+                                            const void* gy, void* gw, void* gbias,
+                                            cudaStream_t stream);
 
 /* Fused multi-branch forward (the DynamicConvolutionOperator's single launch
  * for dilation 1, 3, 5 whose results are stored straight into slices of one
