@@ -260,6 +260,11 @@ def gpu_arm(args, rank, world):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     items = build_workload(args.workload)
+    if args.layers:
+        keep = set(args.layers.split(","))
+        items = [i for i in items if i.label() in keep]
+        if not items:
+            raise SystemExit(f"--layers matched nothing in {args.workload}")
     dist = None
     if world > 1:
         import torch.distributed as dist_
@@ -480,6 +485,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fma-probe", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--layers", default="", help="comma-separated layer labels to keep (profiling runs)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))

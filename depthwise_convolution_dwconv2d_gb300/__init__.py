@@ -8,5 +8,5 @@ seeded synthetic inputs and holds no convolution arithmetic.
 from .binding import (  # noqa: F401
     DTYPES, Desc, DwconvError, ESIZE, SYMBOLS, dwconv2d_bwd_data, dwconv2d_bwd_data_multi,
     dwconv2d_bwd_weight, dwconv2d_bwd_weight_noalloc, dwconv2d_bwd_weight_workspace_size, dwconv2d_fwd, dwconv2d_fwd_multi,
-    dwconv2d_multi_plan_name, dwconv2d_output_shape, dwconv2d_plan_name, dwconv_fma_probe, dwconv_status_string, lib_path,
+    dwconv2d_multi_plan_name, dwconv2d_output_shape, dwconv2d_plan_name, dwconv_device_timeouts, dwconv_fma_probe, dwconv_status_string, lib_path,
     load, make_desc)

@@ -23,7 +23,8 @@ STATUS = {0: "DWCONV_OK", 1: "DWCONV_ERR_INVALID_ARG", 2: "DWCONV_ERR_UNSUPPORTE
 SYMBOLS = ("dwconv2d_output_shape", "dwconv2d_fwd", "dwconv2d_bwd_data",
            "dwconv2d_bwd_weight_workspace_size", "dwconv2d_bwd_weight", "dwconv2d_fwd_multi",
            "dwconv2d_bwd_data_multi", "dwconv_status_string", "dwconv2d_plan_name",
-           "dwconv2d_multi_plan_name", "dwconv_fma_probe", "dwconv2d_bwd_weight_noalloc")
+           "dwconv2d_multi_plan_name", "dwconv_fma_probe", "dwconv2d_bwd_weight_noalloc",
+           "dwconv_device_timeouts")
 
 
 class DwconvError(RuntimeError):
@@ -94,6 +95,7 @@ def load():
     lib.dwconv2d_plan_name.restype = ctypes.c_char_p
     lib.dwconv2d_multi_plan_name.argtypes = [ctypes.c_int, P]
     lib.dwconv2d_multi_plan_name.restype = ctypes.c_char_p
+    lib.dwconv_device_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     lib.dwconv_fma_probe.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp]
     for name in SYMBOLS:
         if name not in ("dwconv2d_bwd_weight_workspace_size", "dwconv_status_string", "dwconv2d_plan_name",
@@ -198,6 +200,12 @@ def dwconv2d_plan_name(desc: Desc, pass_: int) -> str:
 
 def dwconv2d_multi_plan_name(descs) -> str:
     return load().dwconv2d_multi_plan_name(len(descs), _desc_array(descs)).decode()
+
+
+def dwconv_device_timeouts() -> int:
+    n = ctypes.c_uint(0)
+    _check(load().dwconv_device_timeouts(ctypes.byref(n)), "dwconv_device_timeouts")
+    return int(n.value)
 
 
 def dwconv_fma_probe(blocks: int, iters: int, sink, stream=None):

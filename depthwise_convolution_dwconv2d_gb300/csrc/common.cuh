@@ -53,6 +53,32 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
 // plain (coherent) load for data this kernel may also write
 template <typename T> __device__ __forceinline__ float ld_rw(const T* p) { return to_f<T>(*p); }
 
+// Division of 32-bit unsigned numerators by a divisor fixed at launch time,
+// as a multiply-high and two shifts (Granlund and Montgomery, "Division by
+// invariant integers using multiplication", PLDI 1994, section 4): with
+// l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1,
+// t = mulhi(m, n), q = (t + ((n - t) >> 1)) >> (l - 1), exact for all n < 2^32.
+struct FastDiv {
+  uint32_t d, m, s1, s2;
+  FastDiv() = default;
+  __host__ explicit FastDiv(uint32_t div) : d(div) {
+    uint32_t l = 0;
+    while ((uint64_t(1) << l) < div) ++l;
+    m = (uint32_t)(((uint64_t(1) << 32) * ((uint64_t(1) << l) - div)) / div + 1);
+    s1 = l > 0 ? 1u : 0u;
+    s2 = l > 0 ? l - 1 : 0u;
+  }
+  __device__ __forceinline__ uint32_t div(uint32_t n) const {
+    const uint32_t t = __umulhi(m, n);
+    return (t + ((n - t) >> s1)) >> s2;
+  }
+  // q = n / d, returns n - q * d
+  __device__ __forceinline__ uint32_t divmod(uint32_t n, uint32_t& q) const {
+    q = div(n);
+    return n - q * d;
+  }
+};
+
 inline int div_up(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
 // Launch helpers: each family exposes launch functions templated on nothing;

@@ -1,12 +1,19 @@
 // Shared-memory tile machinery for the small-kernel depthwise kernels.
 //
-// A CTA stages a band of input rows (with the halo the kernel needs, zero
-// outside the plane) of one or more channel planes into shared memory as
-// fp32, then every thread computes an R x V block of outputs from it with the
-// filter held in registers and a sliding window of the tile row in registers
-// (the multi-level blocking of the MegEngine large-kernel depthwise article,
-// section "DirectConv": CTA tile -> rows -> a small block of outputs per
+// A CTA stages a band of input rows (with the halo the filter needs, zero
+// outside the plane) of one or more channel planes into shared memory in the
+// storage type, then every thread computes an R x V block of outputs from it
+// with the filter in registers and a sliding window of each tile row in
+// registers (the multi-level blocking of the MegEngine large-kernel depthwise
+// article, section "DirectConv": CTA tile -> rows -> a block of outputs per
 // thread).
+//
+// Staging uses cp.async (asynchronous global->shared copies): 16-byte chunks
+// when every row start and the tile origin are 16-byte aligned, 4-byte chunks
+// otherwise, with zero fill through the copy's source size for chunks outside
+// the plane. The tile kernels are persistent and run two stages: the copies
+// for a CTA's next tile are in flight while it computes the current one, so
+// HBM traffic does not stop at tile boundaries.
 //
 // Output block of a thread: rows oh_b + r*Q, cols ow_b + v*Q (r < R, v < V)
 // with Q = D / S when the dilation is a multiple of the stride, else Q = 1.
@@ -28,170 +35,174 @@ struct Geo {
   static constexpr int QS = Q * S;
 };
 
-// Host/device description of one CTA's tile (computed on the host).
-struct TileCfg {
-  int ppc;       // channel planes per CTA
-  int th;        // output rows per band
-  int nbands;    // bands per plane
-  int tr, pitch; // tile rows and row pitch (floats); pitch % 4 == 0
-  int rb, cb;    // row / col blocks of the item grid
-  int ntile;     // staged planes per output plane (1, or m for bwd_data)
-  int tile_floats;  // floats per staged plane (tr * pitch)
-  int vec_in;    // 16-byte global loads allowed
-  int vec_out;   // V-wide vector stores allowed
-  int64_t groups;   // plane groups (grid = groups * nbands)
-};
+// Copy mode of a tile: 16-byte chunks, 4-byte chunks, or plain loads and
+// stores (2-byte types with odd alignment).
+enum CopyMode { kCopySync = 0, kCopy4 = 1, kCopy16 = 2, kCopyTMA = 3 };
 
-// ---- tile loading ------------------------------------------------------------
-template <typename T> struct Vec16;
-template <> struct Vec16<float> { static constexpr int n = 4; };
-template <> struct Vec16<__half> { static constexpr int n = 8; };
-template <> struct Vec16<__nv_bfloat16> { static constexpr int n = 8; };
-
-template <typename T>
-__device__ __forceinline__ void cvt16(const uint4& u, float* out);
-template <>
-__device__ __forceinline__ void cvt16<float>(const uint4& u, float* out) {
-  out[0] = __uint_as_float(u.x); out[1] = __uint_as_float(u.y);
-  out[2] = __uint_as_float(u.z); out[3] = __uint_as_float(u.w);
+// ---- cp.async ------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
+  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(src_bytes)
+               : "memory");
 }
-template <>
-__device__ __forceinline__ void cvt16<__half>(const uint4& u, float* out) {
-  const __half2* h = reinterpret_cast<const __half2*>(&u);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float2 f = __half22float2(h[i]);
-    out[2 * i] = f.x; out[2 * i + 1] = f.y;
-  }
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem, int src_bytes) {
+  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(s), "l"(gmem), "r"(src_bytes)
+               : "memory");
 }
-template <>
-__device__ __forceinline__ void cvt16<__nv_bfloat16>(const uint4& u, float* out) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    out[2 * i] = __uint_as_float(w[i] << 16);
-    out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-// Stage `np` planes into smem. Plane i comes from src_of(i) (H x W elements,
-// row-major) and lands at dst + i * tile_floats as rows [iy0, iy0 + tr) x
-// cols [ix0, ix0 + cols) with row pitch `pitch`; samples outside the plane
-// are zero. vec: every row start is 16-byte aligned in global memory.
+// Issue the copies that stage `np` planes into smem (no wait). Plane i comes
+// from src_of(i) (H x W elements, row-major) and lands at dst + i*plane_elems
+// as rows [iy0, iy0 + tr) x cols [ix0, ix0 + pitch); samples outside the
+// plane are zero. Copy modes 16 / 4 need ix0 and W to be multiples of the
+// chunk (in elements) and 16- / 4-byte aligned plane bases; pitch is a
+// multiple of 16 bytes. Rows are spread over warps, the lanes of a row sweep
+// its chunks; narrow rows share a warp.
 template <typename T, typename SrcOf>
-__device__ __forceinline__ void load_planes(float* __restrict__ dst, int np, int tile_floats,
-                                            int pitch, SrcOf src_of, int H, int W, int iy0,
-                                            int tr, int ix0, int cols, bool vec) {
-  // rows of the tile that hold plane rows
-  const int r_lo = iy0 < 0 ? -iy0 : 0;
-  const int r_hi = (H - iy0) < tr ? (H - iy0) : tr;
-  const int nrow_in = r_hi > r_lo ? r_hi - r_lo : 0;
-  // columns of the tile that hold plane columns: [c_lo, c_hi)
-  const int c_lo = ix0 < 0 ? (-ix0 < cols ? -ix0 : cols) : 0;
-  const int c_hi0 = (W - ix0) < cols ? (W - ix0) : cols;
-  const int c_hi = c_hi0 > c_lo ? c_hi0 : c_lo;
-  // 1) zero the halo: whole rows outside the plane, and the side columns
-  {
-    const int hl = c_lo, hr = cols - c_hi;  // left / right halo widths
-    const int side = hl + hr;
-    const int nrow_out = tr - nrow_in;
-    const int per_plane = nrow_out * cols + nrow_in * side;
-    for (int e = threadIdx.x; e < np * per_plane; e += blockDim.x) {
-      const int p = e / per_plane;
-      int q = e - p * per_plane;
-      int row, col;
-      if (q < nrow_out * cols) {
-        const int rr = q / cols;
-        col = q - rr * cols;
-        row = rr < r_lo ? rr : rr + nrow_in;
-      } else {
-        q -= nrow_out * cols;
-        const int rr = q / side;
-        const int k = q - rr * side;
-        row = r_lo + rr;
-        col = k < hl ? k : c_hi + (k - hl);
+__device__ __forceinline__ void issue_tile(T* __restrict__ dst, int np, int plane_elems, int pitch,
+                                           SrcOf src_of, int H, int W, int iy0, int tr,
+                                           const FastDiv& trdiv, int ix0, int mode) {
+  constexpr int ES = sizeof(T);
+  const int ce = mode == kCopy16 ? 16 / ES : mode == kCopy4 ? 4 / ES : 1;  // elements per chunk
+  const int nch = pitch / ce;
+  const int lpr = nch > 16 ? 32 : nch > 8 ? 16 : nch > 4 ? 8 : 4;  // lanes per row
+  const int rpw = 32 / lpr;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = lane / lpr, l = lane & (lpr - 1);
+  const int nwarps = blockDim.x >> 5;
+  const int rows = np * tr;
+  for (int q = warp * rpw + sub; q < rows; q += nwarps * rpw) {
+    uint32_t p;
+    const int r = (int)trdiv.divmod((uint32_t)q, p);
+    const int iy = iy0 + r;
+    const bool rin = iy >= 0 && iy < H;
+    T* drow = dst + (int)p * plane_elems + r * pitch;
+    const T* plane = src_of((int)p);
+    const T* srow = plane + (int64_t)(rin ? iy : 0) * W;
+    if (mode == kCopy16) {
+      for (int c = l; c < nch; c += lpr) {
+        const int ix = ix0 + c * ce;
+        const bool in = rin && ix >= 0 && ix + ce <= W;
+        cp_async16(drow + c * ce, in ? srow + ix : plane, in ? 16 : 0);
       }
-      dst[p * tile_floats + row * pitch + col] = 0.f;
-    }
-  }
-  if (nrow_in == 0 || c_hi <= c_lo) return;
-  // 2) copy plane samples in tile columns [c_lo, c_hi), i.e. plane columns
-  //    [c_lo + ix0, c_hi + ix0)
-  constexpr int VN = Vec16<T>::n;
-  if (vec && W % VN == 0 && ix0 <= 0 && W - ix0 <= cols) {
-    const int cpr = W / VN;  // chunks per row
-    const int total = np * nrow_in * cpr;
-    for (int e = threadIdx.x; e < total; e += blockDim.x) {
-      const int p = e / (nrow_in * cpr);
-      const int q = e - p * (nrow_in * cpr);
-      const int rr = q / cpr;
-      const int ch = q - rr * cpr;
-      const int row = r_lo + rr;
-      const T* s = src_of(p) + (int64_t)(iy0 + row) * W + ch * VN;
-      const uint4 u = __ldg(reinterpret_cast<const uint4*>(s));
-      float f[VN];
-      cvt16<T>(u, f);
-      float* d = dst + p * tile_floats + row * pitch + (ch * VN - ix0);
-#pragma unroll
-      for (int i = 0; i < VN; ++i) d[i] = f[i];
-    }
-  } else {
-    const int nc = c_hi - c_lo;
-    const int total = np * nrow_in * nc;
-    for (int e = threadIdx.x; e < total; e += blockDim.x) {
-      const int p = e / (nrow_in * nc);
-      const int q = e - p * (nrow_in * nc);
-      const int rr = q / nc;
-      const int tc = c_lo + (q - rr * nc);
-      const int row = r_lo + rr;
-      dst[p * tile_floats + row * pitch + tc] = ld(src_of(p) + (int64_t)(iy0 + row) * W + (tc + ix0));
+    } else if (mode == kCopy4) {
+      for (int c = l; c < nch; c += lpr) {
+        const int ix = ix0 + c * ce;
+        const bool in = rin && ix >= 0 && ix + ce <= W;
+        cp_async4(drow + c * ce, in ? srow + ix : plane, in ? 4 : 0);
+      }
+    } else {
+      for (int c = l; c < pitch; c += lpr) {
+        const int ix = ix0 + c;
+        drow[c] = (rin && ix >= 0 && ix < W) ? srow[ix] : from_f<T>(0.f);
+      }
     }
   }
 }
+
+// Pick the widest copy mode the planes allow and the tile origin column for
+// it: want_ix0 (the plane column the kernel wants at tile column 0) rounded
+// down to the chunk; *shift = want_ix0 - origin (>= 0) is how far the data
+// sits to the right of where the kernel expects it.
+template <typename T>
+inline int pick_mode(const void* base, int64_t W, int want_ix0, int* ix0, int* shift) {
+  constexpr int ES = sizeof(T);
+  auto floor_to = [](int v, int m) { return v >= 0 ? v / m * m : -((-v + m - 1) / m) * m; };
+  const uintptr_t a = reinterpret_cast<uintptr_t>(base);
+  if ((a % 16) == 0 && (W * ES) % 16 == 0) {
+    *ix0 = floor_to(want_ix0, 16 / ES);
+    *shift = want_ix0 - *ix0;
+    return kCopy16;
+  }
+  if ((a % 4) == 0 && (W * ES) % 4 == 0) {
+    *ix0 = floor_to(want_ix0, 4 / ES);
+    *shift = want_ix0 - *ix0;
+    return kCopy4;
+  }
+  *ix0 = want_ix0;
+  *shift = 0;
+  return kCopySync;
+}
+
+// ---- reading tile values as fp32 -------------------------------------------
+template <typename T>
+__device__ __forceinline__ void ld4(const T* p, float* o);
+template <>
+__device__ __forceinline__ void ld4<float>(const float* p, float* o) {
+  const float4 f = *reinterpret_cast<const float4*>(p);
+  o[0] = f.x; o[1] = f.y; o[2] = f.z; o[3] = f.w;
+}
+template <>
+__device__ __forceinline__ void ld4<__nv_bfloat16>(const __nv_bfloat16* p, float* o) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  o[0] = __uint_as_float(u.x << 16); o[1] = __uint_as_float(u.x & 0xffff0000u);
+  o[2] = __uint_as_float(u.y << 16); o[3] = __uint_as_float(u.y & 0xffff0000u);
+}
+template <>
+__device__ __forceinline__ void ld4<__half>(const __half* p, float* o) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+  o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
+}
+template <typename T>
+__device__ __forceinline__ float ld1(const T* p) { return to_f<T>(*p); }
 
 // ---- the register-blocked stencil ------------------------------------------
+// Which rows u = r*QS + a*D (r < R, a < K) and window columns i = v*QS + b*D
+// (v < V, b < K) a block touches, as bit masks evaluated at compile time (a
+// constexpr function called with an unrolled loop index is not folded, so
+// the masks are computed once into constants and tested with shifts).
+template <int K, int D, int N, int QS>
+struct TapMask {
+  static constexpr uint64_t value = [] {
+    uint64_t m = 0;
+    for (int r = 0; r < N; ++r)
+      for (int a = 0; a < K; ++a) m |= uint64_t(1) << (r * QS + a * D);
+    return m;
+  }();
+  static_assert((N - 1) * QS + (K - 1) * D < 64, "tap mask wider than 64 bits");
+};
+
 template <int K, int D, int R, int QS>
-__device__ constexpr bool row_used(int u) {
-  for (int r = 0; r < R; ++r)
-    for (int a = 0; a < K; ++a)
-      if (r * QS + a * D == u) return true;
-  return false;
+__device__ __forceinline__ constexpr bool row_used(int u) {
+  return (TapMask<K, D, R, QS>::value >> u) & 1;
 }
-
 template <int K, int D, int V, int QS>
-__device__ constexpr bool col_used(int i) {
-  for (int v = 0; v < V; ++v)
-    for (int b = 0; b < K; ++b)
-      if (v * QS + b * D == i) return true;
-  return false;
+__device__ __forceinline__ constexpr bool col_used(int i) {
+  return (TapMask<K, D, V, QS>::value >> i) & 1;
 }
 
-// acc[r][v] += sum_{a,b} wr[a*K+b] * t[(tr0 + r*Q*S + a*D) * pitch + tc0 + v*Q*S + b*D]
-// With Q == 1 the window of a tile row is contiguous and is read with float4
-// loads, so tc0 must then be a multiple of 4.
-template <int K, int S, int D, int R, int V, int Q>
-__device__ __forceinline__ void conv_block(const float* __restrict__ t, int pitch, int tr0, int tc0,
+// acc[r][v] += sum_{a,b} wr[a*K+b] * t[(tr0 + r*Q*S + a*D) * pitch + tc0 + DL + v*Q*S + b*D]
+// With Q == 1 the window of a tile row is contiguous: it is read with 4-wide
+// vector loads starting at tc0, which must then be a multiple of 4, and DL
+// (0..3) is the compile-time offset of the first used value in it. With
+// Q > 1 values are read one by one and DL must be 0 (fold it into tc0).
+template <int K, int S, int D, int R, int V, int Q, int DL, typename TS>
+__device__ __forceinline__ void conv_block(const TS* __restrict__ t, int pitch, int tr0, int tc0,
                                            const float (&wr)[K * K], float (&acc)[R][V]) {
   constexpr int QS = Q * S;
   constexpr bool VEC = Q == 1;
   constexpr int U = (R - 1) * QS + (K - 1) * D + 1;
   constexpr int WN = (V - 1) * QS + (K - 1) * D + 1;
-  constexpr int WN4 = (WN + 3) / 4 * 4;
-  constexpr int WA = VEC ? WN4 : WN;
+  constexpr int W4 = (DL + WN + 3) / 4 * 4;
+  constexpr int WA = VEC ? W4 : WN;
 #pragma unroll
   for (int u = 0; u < U; ++u) {
     if (!row_used<K, D, R, QS>(u)) continue;
-    const float* rowp = t + (tr0 + u) * pitch + tc0;
+    const TS* rowp = t + (tr0 + u) * pitch + tc0;
     float win[WA];
     if (VEC) {
 #pragma unroll
-      for (int i = 0; i < WN4 / 4; ++i) {
-        const float4 f = *reinterpret_cast<const float4*>(rowp + 4 * i);
-        win[4 * i] = f.x; win[4 * i + 1] = f.y; win[4 * i + 2] = f.z; win[4 * i + 3] = f.w;
-      }
+      for (int i = 0; i < W4 / 4; ++i) ld4<TS>(rowp + 4 * i, win + 4 * i);
     } else {
 #pragma unroll
-      for (int i = 0; i < WA; ++i) win[i] = col_used<K, D, V, QS>(i) ? rowp[i] : 0.f;
+      for (int i = 0; i < WA; ++i) win[i] = col_used<K, D, V, QS>(i) ? ld1<TS>(rowp + i) : 0.f;
     }
 #pragma unroll
     for (int r = 0; r < R; ++r) {
@@ -201,7 +212,8 @@ __device__ __forceinline__ void conv_block(const float* __restrict__ t, int pitc
 #pragma unroll
         for (int b = 0; b < K; ++b) {
 #pragma unroll
-          for (int v = 0; v < V; ++v) acc[r][v] = fmaf(wr[a * K + b], win[v * QS + b * D], acc[r][v]);
+          for (int v = 0; v < V; ++v)
+            acc[r][v] = fmaf(wr[a * K + b], win[(VEC ? DL : 0) + v * QS + b * D], acc[r][v]);
         }
       }
     }
@@ -232,8 +244,8 @@ __device__ __forceinline__ void store_vec<__nv_bfloat16, 4>(__nv_bfloat16* p, co
   *reinterpret_cast<uint2*>(p) = u;
 }
 
-// Store an R x V block at rows oh + r*Q (r-th valid while < rows_left),
-// cols ow + v*Q (< Wo). add: read-modify-write (gx += ...).
+// Store an R x V block at rows oh + r*Q (r-th valid while r*Q < rows_left),
+// cols ow + v*Q (< cols). add: read-modify-write (gx += ...).
 template <typename T, int R, int V, int Q>
 __device__ __forceinline__ void store_block(T* __restrict__ plane, int64_t Wo, int oh, int ow,
                                             int rows_left, int cols, float (&acc)[R][V], bool vec,
@@ -243,10 +255,10 @@ __device__ __forceinline__ void store_block(T* __restrict__ plane, int64_t Wo, i
     if (r * Q >= rows_left) break;
     T* rowp = plane + (int64_t)(oh + r * Q) * Wo;
     if (Q == 1 && V == 4 && vec && ow + V <= cols) {
-      float o[V];
+      float o[4];
 #pragma unroll
-      for (int v = 0; v < V; ++v) o[v] = add ? acc[r][v] + ld_rw(rowp + ow + v) : acc[r][v];
-      store_vec<T, 4>(rowp + ow, reinterpret_cast<const float(&)[4]>(o));
+      for (int v = 0; v < 4; ++v) o[v] = add ? acc[r][v] + ld_rw(rowp + ow + v) : acc[r][v];
+      store_vec<T, 4>(rowp + ow, o);
     } else {
 #pragma unroll
       for (int v = 0; v < V; ++v) {
@@ -257,82 +269,29 @@ __device__ __forceinline__ void store_block(T* __restrict__ plane, int64_t Wo, i
   }
 }
 
-}  // namespace tile
-}  // namespace dwconv
+// ---- host-side planning -------------------------------------------------------
+inline int round_up(int64_t v, int m) { return (int)((v + m - 1) / m * m); }
 
-namespace dwconv {
-namespace tile {
+// Stage sizes are kept multiples of 128 bytes (TMA destinations).
+inline int stage_round(int64_t elems, int es) { return (int)((elems * es + 127) / 128 * 128 / es); }
 
-// Geometry of the stencil a tile kernel evaluates, written as a forward
-// convolution: out[oy][ox] = sum_{a,b} w'[a][b] * in[oy*S - ph + a*D][ox*S - pw + b*D]
-// (for bwd_data at stride 1, `in` is grad_out, w' the flipped filter and
-// ph = D*(K-1) - pad).
-struct VGeo {
-  int K, S, D, Q, R, V;
-  int64_t Hin, Win, Hout, Wout;
-  int ph, pw;
-};
-
-inline int round4(int64_t v) { return (int)((v + 3) / 4 * 4); }
-
-// Widest tile column any thread reads (+1), for a row of cb column blocks.
-inline int64_t cols_read(const VGeo& g, int cb) {
-  const int QS = g.Q * g.S;
-  const int WN = (g.V - 1) * QS + (g.K - 1) * g.D + 1;
-  if (g.Q == 1) return (int64_t)(cb - 1) * g.V * g.S + (WN + 3) / 4 * 4;
-  const int64_t owb = (int64_t)(cb - 1) * g.Q * g.V + g.Q - 1;
-  return owb * g.S + (g.V - 1) * QS + (g.K - 1) * g.D + 1;
+// Number of persistent CTAs: every SM's resident capacity, capped by the
+// amount of work.
+template <typename KernelT>
+inline int persistent_grid(KernelT kern, size_t smem, int64_t units) {
+  int dev = 0, sms = 152, per_sm = 1;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kNT, smem) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  const int64_t cap = (int64_t)sms * per_sm;
+  return (int)(units < cap ? units : cap);
 }
 
-// Choose band height, planes per CTA and the smem layout. Returns false when
-// no band of the minimum height fits the shared-memory limit.
-inline bool make_cfg(const VGeo& g, int64_t nplanes, int ntile, int mult, bool vec_in,
-                     bool vec_out, TileCfg* out, int64_t ix_extra_left = 0) {
-  const int QR = g.Q * g.R;
-  TileCfg c{};
-  c.cb = (int)((g.Wout + (int64_t)g.Q * g.V - 1) / ((int64_t)g.Q * g.V));
-  const int64_t need = cols_read(g, c.cb) > g.Win + g.pw + ix_extra_left
-                           ? cols_read(g, c.cb) : g.Win + g.pw + ix_extra_left;
-  c.pitch = round4(need);
-  auto tr_of = [&](int64_t th) { return (th - 1) * g.S + (int64_t)(g.K - 1) * g.D + 1; };
-  const int64_t per_cta = 96 * 1024;  // smem budget per CTA (bytes), two CTAs per SM at least
-  const int64_t th_full = (g.Hout + QR - 1) / QR * QR;
-  int64_t th = th_full;
-  auto bytes_of = [&](int64_t t) { return tr_of(t) * c.pitch * 4 * ntile; };
-  const int64_t target = 40 * 1024;
-  if (bytes_of(th) > target) {
-    th = (target / (c.pitch * 4 * ntile) - (int64_t)(g.K - 1) * g.D - 1) / g.S + 1;
-    th = th / QR * QR;
-    if (th < QR) th = QR;
-    if (bytes_of(th) > per_cta) return false;
-  }
-  c.th = (int)th;
-  c.rb = (int)(th / QR);
-  c.nbands = (int)((g.Hout + th - 1) / th);
-  c.tr = (int)tr_of(th);
-  c.ntile = ntile;
-  c.tile_floats = c.tr * c.pitch;
-  const int64_t items = (int64_t)mult * c.rb * c.cb * g.Q * g.Q;
-  int64_t ppc = 1;
-  if (c.nbands == 1) {
-    ppc = (2 * kNT + items - 1) / items;
-    const int64_t cap = target / bytes_of(th);
-    if (ppc > cap) ppc = cap;
-    // keep at least ~4 CTAs per SM worth of groups
-    const int64_t min_groups = 152 * 4;
-    if ((nplanes + ppc - 1) / ppc < min_groups) ppc = (nplanes + min_groups - 1) / min_groups;
-    if (ppc < 1) ppc = 1;
-  }
-  c.ppc = (int)ppc;
-  c.groups = (nplanes + ppc - 1) / ppc;
-  c.vec_in = vec_in;
-  c.vec_out = vec_out;
-  *out = c;
-  return true;
-}
-
-inline size_t smem_bytes(const TileCfg& c) {
-  return (size_t)c.ppc * c.ntile * c.tile_floats * sizeof(float);
+template <typename KernelT>
+inline cudaError_t set_smem(KernelT kern, size_t smem) {
+  if (smem <= 48 * 1024) return cudaSuccess;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
 }  // namespace tile

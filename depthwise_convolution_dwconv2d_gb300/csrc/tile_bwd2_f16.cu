@@ -1,0 +1,8 @@
+// bwd2 tile kernels for __half storage.
+#include "tile_bwd2_impl.cuh"
+
+namespace dwconv {
+namespace tile {
+template cudaError_t bwd2_t<__half>(const Conv&, const void*, const void*, void*, bool, cudaStream_t);
+}  // namespace tile
+}  // namespace dwconv

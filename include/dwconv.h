@@ -182,6 +182,14 @@ const char* dwconv2d_plan_name(const dwconv2d_desc_t* desc, int pass);
  * the grad-input), or "invalid". Host only. */
 const char* dwconv2d_multi_plan_name(int nbranch, const dwconv2d_desc_t* descs);
 
+/* Health check: the number of bounded waits in the library's kernels that
+ * gave up since the library was loaded on the current device (0 in a healthy
+ * run). Tile copies that use the tensor memory accelerator are waited for
+ * with an iteration limit; a wait that runs out increments this counter and
+ * the kernel stops early instead of hanging, leaving its outputs incomplete.
+ * Synchronous: copies the counter to *count. */
+dwconv_status_t dwconv_device_timeouts(unsigned int* count);
+
 /* Measurement helper, not part of the convolution: runs a register-only
  * fp32 FMA loop on every SM (`blocks` x 256 threads, `iters` iterations of 16
  * independent FMA chains) and writes one float per thread to `sink`

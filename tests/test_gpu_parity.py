@@ -326,3 +326,8 @@ def test_generic_and_planned_kernels_agree():
     for u, v in zip(a, b):
         if u is not None:
             assert_close(u, v, L.dtype, 9, "planned vs generic")
+
+
+def test_no_bounded_wait_gave_up():
+    """Every tile copy the suite waited for arrived (no timeouts counted)."""
+    assert B.dwconv_device_timeouts() == 0
