@@ -37,7 +37,7 @@ struct Geo {
 
 // Copy mode of a tile: 16-byte chunks, 4-byte chunks, or plain loads and
 // stores (2-byte types with odd alignment).
-enum CopyMode { kCopySync = 0, kCopy4 = 1, kCopy16 = 2, kCopyTMA = 3 };
+enum CopyMode { kCopySync = 0, kCopy4 = 1, kCopy16 = 2, kCopyTMA = 3, kCopyDense = 4 };
 
 // ---- cp.async ------------------------------------------------------------------
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
@@ -103,6 +103,64 @@ __device__ __forceinline__ void issue_tile(T* __restrict__ dst, int np, int plan
       }
     }
   }
+}
+
+// Dense staging for planes whose rows are not 16-byte multiples (small
+// planes): each plane's H*W contiguous elements are copied with 16-byte
+// cp.async chunks into a staging segment of `seg` elements, starting at the
+// plane's own offset within its 16-byte chunk (its address mod 16); the last
+// chunk is cut at the plane's end by the copy's source size, so nothing
+// outside the plane's 16-byte neighbourhood is read. repitch() then moves the
+// samples into the padded tile layout.
+template <typename T, typename SrcOf>
+__device__ __forceinline__ void issue_flat(T* __restrict__ stg, int np, int seg, SrcOf src_of, int HW) {
+  constexpr int ES = sizeof(T);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  for (int p = warp; p < np; p += nwarps) {
+    const char* a = reinterpret_cast<const char*>(src_of(p));
+    const char* a0 = reinterpret_cast<const char*>(reinterpret_cast<uintptr_t>(a) & ~uintptr_t(15));
+    const char* end = a + (int64_t)HW * ES;
+    const int nch = (int)((end - a0 + 15) / 16);
+    char* d = reinterpret_cast<char*>(stg + p * seg);
+    for (int k = lane; k < nch; k += 32) {
+      const int64_t left = end - (a0 + 16 * k);
+      cp_async16(d + 16 * k, a0 + 16 * k, left >= 16 ? 16 : (int)left);
+    }
+  }
+}
+
+template <typename T, typename SrcOf>
+__device__ __forceinline__ void repitch(T* __restrict__ dst, int np, int plane_elems, int pitch,
+                                        const T* __restrict__ stg, int seg, SrcOf src_of, int H, int W,
+                                        int iy0, int tr, const FastDiv& trdiv, int ix0) {
+  constexpr int ES = sizeof(T);
+  const int lpr = pitch > 16 ? 32 : pitch > 8 ? 16 : pitch > 4 ? 8 : 4;
+  const int rpw = 32 / lpr;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = lane / lpr, l = lane & (lpr - 1);
+  const int nwarps = blockDim.x >> 5;
+  for (int q = warp * rpw + sub; q < np * tr; q += nwarps * rpw) {
+    uint32_t p;
+    const int r = (int)trdiv.divmod((uint32_t)q, p);
+    const int iy = iy0 + r;
+    const bool rin = iy >= 0 && iy < H;
+    const int mo = (int)((reinterpret_cast<uintptr_t>(src_of((int)p)) & 15) / ES);
+    const T* srow = stg + (int)p * seg + mo + (rin ? iy : 0) * W;
+    T* drow = dst + (int)p * plane_elems + r * pitch;
+    for (int c = l; c < pitch; c += lpr) {
+      const int ix = ix0 + c;
+      drow[c] = (rin && ix >= 0 && ix < W) ? srow[ix] : from_f<T>(0.f);
+    }
+  }
+}
+
+// Segment size (elements) of one densely staged plane: room for the
+// in-chunk offset and the rounding of the last chunk.
+template <typename T>
+inline int dense_seg(int64_t HW) {
+  constexpr int CE = 16 / sizeof(T);
+  return (int)((HW + 2 * CE + CE - 1) / CE * CE);
 }
 
 // Pick the widest copy mode the planes allow and the tile origin column for
@@ -218,6 +276,50 @@ __device__ __forceinline__ void conv_block(const TS* __restrict__ t, int pitch, 
       }
     }
   }
+}
+
+// Same stencil read straight from a densely staged plane (H x W, row-major)
+// with zero outside it: iy0 / ix0 are the plane row / column of tap (0, 0) of
+// output (0, 0) of the block. Rows outside the plane contribute nothing and
+// are skipped; columns outside it read as zero.
+template <int K, int S, int D, int R, int V, int Q, typename TS>
+__device__ __forceinline__ void conv_block_dense(const TS* __restrict__ plane, int H, int W, int iy0, int ix0,
+                                                 const float (&wr)[K * K], float (&acc)[R][V]) {
+  constexpr int QS = Q * S;
+  constexpr int U = (R - 1) * QS + (K - 1) * D + 1;
+  constexpr int WN = (V - 1) * QS + (K - 1) * D + 1;
+  bool cin[WN];
+#pragma unroll
+  for (int i = 0; i < WN; ++i) cin[i] = col_used<K, D, V, QS>(i) && (unsigned)(ix0 + i) < (unsigned)W;
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    if (!row_used<K, D, R, QS>(u)) continue;
+    const int iy = iy0 + u;
+    if ((unsigned)iy >= (unsigned)H) continue;
+    const TS* rowp = plane + iy * W + ix0;
+    float win[WN];
+#pragma unroll
+    for (int i = 0; i < WN; ++i) win[i] = cin[i] ? ld1<TS>(rowp + i) : 0.f;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+#pragma unroll
+      for (int a = 0; a < K; ++a) {
+        if (r * QS + a * D != u) continue;
+#pragma unroll
+        for (int b = 0; b < K; ++b) {
+#pragma unroll
+          for (int v = 0; v < V; ++v) acc[r][v] = fmaf(wr[a * K + b], win[v * QS + b * D], acc[r][v]);
+        }
+      }
+    }
+  }
+}
+
+// Start of a densely staged plane: segment p plus the plane's own offset in
+// its 16-byte chunk.
+template <typename T>
+__device__ __forceinline__ const T* dense_plane(const T* stg, int seg, int p, const T* src) {
+  return stg + p * seg + (int)((reinterpret_cast<uintptr_t>(src) & 15) / sizeof(T));
 }
 
 // ---- output stores ---------------------------------------------------------

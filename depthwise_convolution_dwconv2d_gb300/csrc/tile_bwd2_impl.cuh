@@ -48,6 +48,7 @@ struct Bwd2Cfg {
   int cshift;       // added to each thread's window start column
   FastDiv trdiv, d_plane, d_cb, d_bands;
   uint32_t tma_bytes;
+  int seg, stg_elems;  // dense staging of whole grad_out planes
 };
 
 template <typename T, int K, int S, int D, int PM, int R, int V, int DL>
@@ -69,14 +70,25 @@ bwd2_kernel(Conv c, Bwd2Cfg g, const __grid_constant__ CUtensorMap tmap, unsigne
   constexpr int W4 = (DL + V + SP + 3) / 4 * 4;
   T* const buf0 = reinterpret_cast<T*>(smraw);
   T* const buf1 = buf0 + g.stage_elems;
+  T* const stg0 = buf1 + g.stage_elems;
+  T* const stg1 = stg0 + g.stg_elems;
   const int64_t nplanes = c.N * c.C;
   const int64_t units = g.groups * g.nbands;
   const int m = c.m;
-  auto issue = [&](int64_t u, T* dst, uint64_t* bar) {
+  auto gy_plane = [&](int64_t p0, int s) {
+    const int pl = s / m, j = s - pl * m;
+    const int64_t pin = p0 + pl, n = pin / c.C, ch = pin - n * c.C;
+    return gy + c.y_base(n, ch * m + j);
+  };
+  auto issue = [&](int64_t u, T* dst, T* stg, uint64_t* bar) {
     uint32_t grp;
     const int band = (int)g.d_bands.divmod((uint32_t)u, grp);
     const int64_t p0 = (int64_t)grp * g.ppc;
     const int np = (int)((nplanes - p0) < g.ppc ? (nplanes - p0) : g.ppc);
+    if (g.mode == kCopyDense) {
+      issue_flat<T>(stg, np * m, g.seg, [&](int s) { return gy_plane(p0, s); }, (int)(c.Ho * c.Wo));
+      return;
+    }
     if (use_tma) {
       if (threadIdx.x == 0) {
         const int64_t n = p0 / c.C, ch = p0 - n * c.C;  // units never straddle samples
@@ -95,12 +107,12 @@ bwd2_kernel(Conv c, Bwd2Cfg g, const __grid_constant__ CUtensorMap tmap, unsigne
                   (int)c.Ho, (int)c.Wo, band * g.thu + g.row0, g.tr, g.trdiv, g.ix0, g.mode);
   };
   int64_t u = blockIdx.x;
-  if (u < units) issue(u, buf0, &bars[0]);
+  if (u < units) issue(u, buf0, stg0, &bars[0]);
   cp_async_commit();
   for (int k = 0; u < units; ++k, u += gridDim.x) {
-    const T* cur = (k & 1) ? buf1 : buf0;
+    T* cur = (k & 1) ? buf1 : buf0;
     const bool more = u + gridDim.x < units;
-    if (more) issue(u + gridDim.x, (k & 1) ? buf0 : buf1, &bars[(k + 1) & 1]);
+    if (more) issue(u + gridDim.x, (k & 1) ? buf0 : buf1, (k & 1) ? stg0 : stg1, &bars[(k + 1) & 1]);
     cp_async_commit();
     cp_async_wait<1>();
     if (use_tma && !tma::mbar_wait(&bars[k & 1], (uint32_t)(k >> 1) & 1, timeouts)) {
@@ -113,6 +125,12 @@ bwd2_kernel(Conv c, Bwd2Cfg g, const __grid_constant__ CUtensorMap tmap, unsigne
     const int64_t p0 = (int64_t)grp * g.ppc;
     const int np = (int)((nplanes - p0) < g.ppc ? (nplanes - p0) : g.ppc);
     const int u0 = band * g.thu;  // first u row of the band (gx row S*u0)
+    if (g.mode == kCopyDense) {
+      repitch<T>(cur, np * m, g.tile_elems, g.pitch, (k & 1) ? stg1 : stg0, g.seg,
+                 [&](int s) { return gy_plane(p0, s); }, (int)c.Ho, (int)c.Wo, u0 + g.row0, g.tr, g.trdiv,
+                 g.ix0);
+      __syncthreads();
+    }
     const int total = np * (int)g.d_plane.d;
     float wr[K * K];
     int cur_pl = -1;
@@ -204,7 +222,7 @@ template <typename T, int K, int S, int D, int PM, int DL>
 cudaError_t launch_bwd2(const Conv& c, const Bwd2Cfg& g, const CUtensorMap& map, const void* gy,
                         const void* w, void* gx, bool acc, cudaStream_t s) {
   auto kern = bwd2_kernel<T, K, S, D, PM, 2, 4, DL>;
-  const size_t smem = 128 + 2 * (size_t)g.stage_elems * sizeof(T);
+  const size_t smem = 128 + 2 * ((size_t)g.stage_elems + g.stg_elems) * sizeof(T);
   cudaError_t e = set_smem(kern, smem);
   if (e != cudaSuccess) return e;
   const int grid = persistent_grid(kern, smem, g.groups * g.nbands);
@@ -255,6 +273,19 @@ cudaError_t run_bwd2_t(const Conv& c, const void* gy, const void* w, void* gx, b
     if (ppc > cap) ppc = cap;
     if (ppc < 1) ppc = 1;
   }
+  // dense staging of whole planes when grad_out rows are not 16-byte multiples
+  if ((g.mode == kCopy4 || g.mode == kCopySync) && g.nbands == 1 &&
+      (reinterpret_cast<uintptr_t>(gy) % 16) == 0) {
+    const int seg = dense_seg<T>(c.Ho * c.Wo);
+    const int64_t per = ((int64_t)g.tile_elems + seg) * ES * c.m;
+    int64_t dppc = (2 * kNT + items - 1) / items;
+    if (dppc > target / per) dppc = target / per;
+    if (dppc >= 1) {
+      g.mode = kCopyDense;
+      g.seg = seg;
+      ppc = dppc;
+    }
+  }
   alignas(64) CUtensorMap map{};
   bool tma = g.mode == kCopy16 && g.pitch <= 256 && g.tr <= 256 && ppc * c.m <= 256;
   if (tma) {
@@ -266,6 +297,7 @@ cudaError_t run_bwd2_t(const Conv& c, const void* gy, const void* w, void* gx, b
   g.groups = (nplanes + ppc - 1) / ppc;
   g.stage_elems = stage_round((int64_t)g.ppc * c.m * g.tile_elems, ES);
   g.tma_bytes = (uint32_t)((int64_t)g.ppc * c.m * g.tile_elems * ES);
+  g.stg_elems = g.mode == kCopyDense ? stage_round((int64_t)g.ppc * c.m * g.seg, ES) : 0;
   g.vec_out = (reinterpret_cast<uintptr_t>(gx) % (4 * ES) == 0) && c.W % 4 == 0;
   switch (dl) {
     case 0: return launch_bwd2<T, K, S, D, PM, 0>(c, g, map, gy, w, gx, acc, s);

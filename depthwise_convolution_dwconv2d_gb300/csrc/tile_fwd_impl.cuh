@@ -42,14 +42,16 @@ fwd_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned int
   __syncthreads();
   T* const buf0 = reinterpret_cast<T*>(smraw);
   T* const buf1 = buf0 + g.stage_elems;
+  T* const stg0 = buf1 + g.stage_elems;  // dense staging (empty unless kCopyDense)
+  T* const stg1 = stg0 + g.stg_elems;
   // per stage: filter taps, bias and output-plane offset of each output plane
-  float* const tab0 = reinterpret_cast<float*>(buf1 + g.stage_elems);
+  float* const tab0 = reinterpret_cast<float*>(stg1 + g.stg_elems);
   float* const tab1 = tab0 + g.tab_floats;
   const int64_t nplanes = c.N * c.C;
   const int64_t units = g.groups * g.nbands;
   const int64_t HW = c.H * c.W;
   const int nout = g.ppc * c.m;  // output planes per full unit
-  auto issue = [&](int64_t u, T* dst, float* tab, uint64_t* bar) {
+  auto issue = [&](int64_t u, T* dst, T* stg, float* tab, uint64_t* bar) {
     uint32_t grp;
     const int band = (int)g.d_bands.divmod((uint32_t)u, grp);
     const int64_t p0 = (int64_t)grp * g.ppc;
@@ -60,6 +62,8 @@ fwd_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned int
         tma::mbar_expect_tx(bar, g.tma_bytes);
         tma::load_3d(dst, &tmap, g.ix0, band * g.th * S - c.ph, (int)p0, bar);
       }
+    } else if (g.mode == kCopyDense) {
+      issue_flat<T>(stg, np, g.seg, [&](int p) { return x + (p0 + p) * HW; }, (int)HW);
     } else {
       issue_tile<T>(dst, np, g.tile_elems, g.pitch, [&](int p) { return x + (p0 + p) * HW; },
                     (int)c.H, (int)c.W, band * g.th * S - c.ph, g.tr, g.trdiv, g.ix0, g.mode);
@@ -82,13 +86,14 @@ fwd_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned int
     }
   };
   int64_t u = blockIdx.x;
-  if (u < units) issue(u, buf0, tab0, &bars[0]);
+  if (u < units) issue(u, buf0, stg0, tab0, &bars[0]);
   cp_async_commit();
   for (int k = 0; u < units; ++k, u += gridDim.x) {
-    const T* cur = (k & 1) ? buf1 : buf0;
+    T* cur = (k & 1) ? buf1 : buf0;
     const float* tab = (k & 1) ? tab1 : tab0;
     const bool more = u + gridDim.x < units;
-    if (more) issue(u + gridDim.x, (k & 1) ? buf0 : buf1, (k & 1) ? tab0 : tab1, &bars[(k + 1) & 1]);
+    if (more) issue(u + gridDim.x, (k & 1) ? buf0 : buf1, (k & 1) ? stg0 : stg1, (k & 1) ? tab0 : tab1,
+                    &bars[(k + 1) & 1]);
     cp_async_commit();
     cp_async_wait<1>();
     if (use_tma && !tma::mbar_wait(&bars[k & 1], (uint32_t)(k >> 1) & 1, timeouts)) {
@@ -101,6 +106,7 @@ fwd_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned int
     const int band = (int)g.d_bands.divmod((uint32_t)u, grp);
     const int64_t p0 = (int64_t)grp * g.ppc;
     const int np = (int)((nplanes - p0) < g.ppc ? (nplanes - p0) : g.ppc);
+    const T* stg = (k & 1) ? stg1 : stg0;
     const int oh0 = band * g.th;
     const int band_rows = (int)((c.Ho - oh0) < g.th ? (c.Ho - oh0) : g.th);
     const float* wt = tab;
@@ -126,7 +132,13 @@ fwd_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned int
       for (int r = 0; r < R; ++r)
 #pragma unroll
         for (int v = 0; v < V; ++v) acc[r][v] = bv;
-      conv_block<K, S, D, R, V, Q, DL>(cur + (pj / c.m) * g.tile_elems, g.pitch, ohr * S, owb * S + g.cshift, wr, acc);
+      if (g.mode == kCopyDense) {
+        const int pl = pj / c.m;
+        conv_block_dense<K, S, D, R, V, Q>(dense_plane(stg, g.seg, pl, x + (p0 + pl) * HW), (int)c.H, (int)c.W,
+                                           ohr * S - c.ph, owb * S - c.pw, wr, acc);
+      } else {
+        conv_block<K, S, D, R, V, Q, DL>(cur + (pj / c.m) * g.tile_elems, g.pitch, ohr * S, owb * S + g.cshift, wr, acc);
+      }
       store_block<T, R, V, Q>(y + ot[pj], c.Wo, oh0 + ohr, owb, band_rows - ohr, (int)c.Wo, acc,
                               g.vec_out, false);
     }
@@ -152,19 +164,28 @@ bwd1_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned in
   __syncthreads();
   T* const buf0 = reinterpret_cast<T*>(smraw);
   T* const buf1 = buf0 + g.stage_elems;
+  T* const stg0 = buf1 + g.stage_elems;  // dense staging (empty unless kCopyDense)
+  T* const stg1 = stg0 + g.stg_elems;
   // per stage: rotated filters of each (gx plane, j) and each gx plane's offset
-  float* const tab0 = reinterpret_cast<float*>(buf1 + g.stage_elems);
+  float* const tab0 = reinterpret_cast<float*>(stg1 + g.stg_elems);
   float* const tab1 = tab0 + g.tab_floats;
   const int64_t nplanes = c.N * c.C;
   const int64_t units = g.groups * g.nbands;
   const int m = c.m;
-  auto issue = [&](int64_t u, T* dst, float* tab, uint64_t* bar) {
+  auto gy_plane = [&](int64_t p0, int s) {
+    const int pl = s / m, j = s - pl * m;
+    const int64_t pin = p0 + pl, n = pin / c.C, ch = pin - n * c.C;
+    return gy + c.y_base(n, ch * m + j);
+  };
+  auto issue = [&](int64_t u, T* dst, T* stg, float* tab, uint64_t* bar) {
     uint32_t grp;
     const int band = (int)g.d_bands.divmod((uint32_t)u, grp);
     const int64_t p0 = (int64_t)grp * g.ppc;
     const int np = (int)((nplanes - p0) < g.ppc ? (nplanes - p0) : g.ppc);
     // staged plane s = pl * m + j holds gy[n, off + c*m + j]
-    if (use_tma) {
+    if (g.mode == kCopyDense) {
+      issue_flat<T>(stg, np * m, g.seg, [&](int s) { return gy_plane(p0, s); }, (int)(c.Ho * c.Wo));
+    } else if (use_tma) {
       if (threadIdx.x == 0) {
         const int64_t n = p0 / c.C, ch = p0 - n * c.C;  // units never straddle samples
         tma::fence_async_smem();
@@ -190,13 +211,14 @@ bwd1_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned in
     for (int pl = threadIdx.x; pl < np; pl += kNT) ot[pl] = (p0 + pl) * c.H * c.W;
   };
   int64_t u = blockIdx.x;
-  if (u < units) issue(u, buf0, tab0, &bars[0]);
+  if (u < units) issue(u, buf0, stg0, tab0, &bars[0]);
   cp_async_commit();
   for (int k = 0; u < units; ++k, u += gridDim.x) {
-    const T* cur = (k & 1) ? buf1 : buf0;
+    T* cur = (k & 1) ? buf1 : buf0;
     const float* tab = (k & 1) ? tab1 : tab0;
     const bool more = u + gridDim.x < units;
-    if (more) issue(u + gridDim.x, (k & 1) ? buf0 : buf1, (k & 1) ? tab0 : tab1, &bars[(k + 1) & 1]);
+    if (more) issue(u + gridDim.x, (k & 1) ? buf0 : buf1, (k & 1) ? stg0 : stg1, (k & 1) ? tab0 : tab1,
+                    &bars[(k + 1) & 1]);
     cp_async_commit();
     cp_async_wait<1>();
     if (use_tma && !tma::mbar_wait(&bars[k & 1], (uint32_t)(k >> 1) & 1, timeouts)) {
@@ -208,6 +230,7 @@ bwd1_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned in
     const int band = (int)g.d_bands.divmod((uint32_t)u, grp);
     const int64_t p0 = (int64_t)grp * g.ppc;
     const int np = (int)((nplanes - p0) < g.ppc ? (nplanes - p0) : g.ppc);
+    const T* stg = (k & 1) ? stg1 : stg0;
     const int ih0 = band * g.th;
     const int band_rows = (int)((c.H - ih0) < g.th ? (c.H - ih0) : g.th);
     const int64_t* ot = reinterpret_cast<const int64_t*>(tab + g.tab_off64);
@@ -231,7 +254,13 @@ bwd1_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned in
         float wr[K * K];
 #pragma unroll
         for (int i = 0; i < K * K; ++i) wr[i] = tab[(pl * m + j) * (K * K) + i];
-        conv_block<K, 1, D, R, V, Q, DL>(cur + (pl * m + j) * g.tile_elems, g.pitch, ihr, iwb + g.cshift, wr, acc);
+        if (g.mode == kCopyDense) {
+          const int sp = pl * m + j;
+          conv_block_dense<K, 1, D, R, V, Q>(dense_plane(stg, g.seg, sp, gy_plane(p0, sp)), (int)c.Ho,
+                                             (int)c.Wo, ihr - qh, iwb - (D * (K - 1) - c.pw), wr, acc);
+        } else {
+          conv_block<K, 1, D, R, V, Q, DL>(cur + (pl * m + j) * g.tile_elems, g.pitch, ihr, iwb + g.cshift, wr, acc);
+        }
       }
       store_block<T, R, V, Q>(gx + ot[pl], c.W, ih0 + ihr, iwb, band_rows - ihr, (int)c.W, acc,
                               g.vec_out, accumulate);
@@ -248,7 +277,7 @@ cudaError_t launch_fwd(const Conv& c, const Cfg& g, const CUtensorMap& map, cons
                        const void* b, void* y, cudaStream_t s) {
   constexpr int R = Blk<K, S>::R, V = Blk<K, S>::V;
   auto kern = fwd_kernel<T, K, S, D, R, V, DL>;
-  const size_t smem = 128 + 2 * (size_t)g.stage_elems * sizeof(T) + 2 * (size_t)g.tab_floats * 4;
+  const size_t smem = 128 + 2 * ((size_t)g.stage_elems + g.stg_elems) * sizeof(T) + 2 * (size_t)g.tab_floats * 4;
   cudaError_t e = set_smem(kern, smem);
   if (e != cudaSuccess) return e;
   const int grid = persistent_grid(kern, smem, g.groups * g.nbands);
@@ -280,7 +309,7 @@ cudaError_t launch_bwd1(const Conv& c, const Cfg& g, const CUtensorMap& map, int
                         const void* w, void* gx, bool acc, cudaStream_t s) {
   constexpr int R = Blk<K, 1>::R, V = Blk<K, 1>::V;
   auto kern = bwd1_kernel<T, K, D, R, V, DL>;
-  const size_t smem = 128 + 2 * (size_t)g.stage_elems * sizeof(T) + 2 * (size_t)g.tab_floats * 4;
+  const size_t smem = 128 + 2 * ((size_t)g.stage_elems + g.stg_elems) * sizeof(T) + 2 * (size_t)g.tab_floats * 4;
   cudaError_t e = set_smem(kern, smem);
   if (e != cudaSuccess) return e;
   const int grid = persistent_grid(kern, smem, g.groups * g.nbands);

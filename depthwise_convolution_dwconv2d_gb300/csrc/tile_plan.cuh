@@ -26,6 +26,8 @@ struct Cfg {
   int64_t groups;
   FastDiv trdiv, d_item, d_rb, d_cbq, d_bands;
   uint32_t tma_bytes;  // bytes one stage's tensor copy delivers
+  int seg;             // dense staging: elements per plane segment
+  int stg_elems;       // dense staging: elements per stage (0 otherwise)
 };
 
 
@@ -88,6 +90,25 @@ bool plan_tile(int64_t nplanes, int ntile, int mult, int64_t Hin, int64_t Win, i
     if (ppc > cap) ppc = cap;
     if (ppc < 1) ppc = 1;
   }
+  // dense staging of whole planes when the rows are not 16-byte multiples
+  // but the plane bases are (planes of 16-byte multiples), and a plane is
+  // one band
+  const bool dense_ok = (g.mode == kCopy4 || g.mode == kCopySync) && g.nbands == 1 &&
+                        (reinterpret_cast<uintptr_t>(in_base) % 16) == 0;
+  if (dense_ok) {
+    const int seg = dense_seg<T>(Hin * Win);
+    const int64_t per = (int64_t)seg * ntile * ES;  // dense planes are read in place
+    int64_t dppc = (2 * kNT + items - 1) / items;
+    const int64_t dcap = target / per;
+    if (dppc > dcap) dppc = dcap;
+    if (dppc >= 1) {
+      g.mode = kCopyDense;
+      g.seg = seg;
+      ppc = dppc;
+      // plane groups of a unit never straddle samples (staged planes are
+      // addressed per plane, so this only keeps units uniform)
+    }
+  }
   // TMA staging when the rows allow 16-byte copies and the box fits
   bool tma = g.mode == kCopy16 && g.pitch <= 256 && g.tr <= 256 && ppc * ntile <= 256;
   if (tma && tma_group > 0) {
@@ -101,8 +122,9 @@ bool plan_tile(int64_t nplanes, int ntile, int mult, int64_t Hin, int64_t Win, i
   if (tma) g.mode = kCopyTMA;
   g.ppc = (int)ppc;
   g.groups = (nplanes + ppc - 1) / ppc;
-  g.stage_elems = stage_round((int64_t)g.ppc * ntile * g.tile_elems, ES);
+  g.stage_elems = g.mode == kCopyDense ? 0 : stage_round((int64_t)g.ppc * ntile * g.tile_elems, ES);
   g.tma_bytes = (uint32_t)((int64_t)g.ppc * ntile * g.tile_elems * ES);
+  g.stg_elems = g.mode == kCopyDense ? stage_round((int64_t)g.ppc * ntile * g.seg, ES) : 0;
   // side table: K*K filter taps per staged plane (per output plane for the
   // forward: mult * ppc of them), one bias each, one 64-bit offset each
   const int ntab = g.ppc * (ntile > mult ? ntile : mult);

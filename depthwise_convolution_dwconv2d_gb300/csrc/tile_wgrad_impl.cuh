@@ -41,6 +41,8 @@ struct WCfg {
   int tma;                  // stage with tensor copies (x and grad_out maps)
   uint32_t tma_bytes;       // bytes per full stage (one band per plane)
   uint32_t tma_slice_bytes; // bytes per slice (banded planes)
+  int xseg, gseg;           // dense staging segment sizes (x, grad_out)
+  int stg_off, gstg_off;    // element offsets of the dense staging regions in a stage
   FastDiv trdiv, thdiv, d_per, d_cb;
 };
 
@@ -80,6 +82,24 @@ wgrad_kernel(Conv c, WCfg g, const __grid_constant__ CUtensorMap xmap,
     const int ns = (nsl - s0) < g.ppc ? (nsl - s0) : g.ppc;
     T* xs = dst;
     T* gs = dst + g.goff;
+    if (!g.tma && (g.xmode == kCopyDense || g.gmode == kCopyDense)) {
+      // whole planes (one band): x and grad_out each dense or row-wise
+      if (g.xmode == kCopyDense)
+        issue_flat<T>(dst + g.stg_off, ns, g.xseg, [&](int q) { return x + c.x_base(n0 + s0 + q, ch); },
+                      (int)(c.H * c.W));
+      else
+        issue_tile<T>(xs, ns, g.xstride, g.pitch, [&](int q) { return x + c.x_base(n0 + s0 + q, ch); },
+                      (int)c.H, (int)c.W, -c.ph, g.tr, g.trdiv, g.xix0, g.xmode);
+      if (g.gmode == kCopyDense)
+        issue_flat<T>(dst + g.gstg_off, ns * M, g.gseg,
+                      [&](int qj) { return gy + c.y_base(n0 + s0 + qj / M, ch * M + qj % M); },
+                      (int)(c.Ho * c.Wo));
+      else
+        issue_tile<T>(gs, ns * M, g.g_elems, g.gpitch,
+                      [&](int qj) { return gy + c.y_base(n0 + s0 + qj / M, ch * M + qj % M); },
+                      (int)c.Ho, (int)c.Wo, 0, g.th, g.thdiv, 0, g.gmode);
+      return;
+    }
     if (g.tma) {
       if (threadIdx.x == 0) {
         tma::fence_async_smem();
@@ -147,10 +167,13 @@ wgrad_kernel(Conv c, WCfg g, const __grid_constant__ CUtensorMap xmap,
       return;
     }
     __syncthreads();
-    const T* xs = (k & 1) ? buf[1] : buf[0];
+    T* const cbuf = (k & 1) ? buf[1] : buf[0];
+    const T* xs = cbuf;
     const T* gs = xs + g.goff;
     const int nsl = unit_slices(u);
     const int ns = (nsl - s0) < g.ppc ? (nsl - s0) : g.ppc;
+    const int64_t chu = u % c.C;
+    const int64_t n0u = (u / c.C) * g.nb;
     const int per = (int)g.d_per.d;
     for (int it = threadIdx.x; it < ns * per; it += kNT) {
       uint32_t q_, rbi_;
@@ -158,23 +181,54 @@ wgrad_kernel(Conv c, WCfg g, const __grid_constant__ CUtensorMap xmap,
       const int cbi = (int)g.d_cb.divmod(rem, rbi_);
       const int q = (int)q_, rbi = (int)rbi_;
       float gv[M][R][V];
+      if (g.gmode == kCopyDense) {
 #pragma unroll
-      for (int j = 0; j < M; ++j)
+        for (int j = 0; j < M; ++j) {
+          const T* gp = dense_plane(cbuf + g.gstg_off, g.gseg, q * M + j,
+                                    gy + c.y_base(n0u + s0 + q, chu * M + j));
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-          float f[4];
-          ld4<T>(gs + q * g.gstride + j * g.g_elems + (rbi * R + r) * g.gpitch + cbi * V, f);
+          for (int r = 0; r < R; ++r) {
+            const int oh = rbi * R + r;
 #pragma unroll
-          for (int v = 0; v < V; ++v) gv[j][r][v] = f[v];
-          acc[j][KK] += (f[0] + f[1]) + (f[2] + f[3]);
+            for (int v = 0; v < V; ++v) {
+              const int ow = cbi * V + v;
+              gv[j][r][v] = (oh < c.Ho && ow < c.Wo) ? ld1<T>(gp + oh * c.Wo + ow) : 0.f;
+            }
+            acc[j][KK] += (gv[j][r][0] + gv[j][r][1]) + (gv[j][r][2] + gv[j][r][3]);
+          }
         }
+      } else {
+#pragma unroll
+        for (int j = 0; j < M; ++j)
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            float f[4];
+            ld4<T>(gs + q * g.gstride + j * g.g_elems + (rbi * R + r) * g.gpitch + cbi * V, f);
+#pragma unroll
+            for (int v = 0; v < V; ++v) gv[j][r][v] = f[v];
+            acc[j][KK] += (f[0] + f[1]) + (f[2] + f[3]);
+          }
+      }
+      const bool xd = g.xmode == kCopyDense;
+      const T* xp = xd ? dense_plane(cbuf + g.stg_off, g.xseg, q, x + c.x_base(n0u + s0 + q, chu)) : nullptr;
+      const int iyb = rbi * R * S - c.ph, ixb = cbi * V * S - c.pw;  // dense: plane coordinates
+      bool cin[WN];
+#pragma unroll
+      for (int i = 0; i < WN; ++i) cin[i] = (unsigned)(ixb + i) < (unsigned)c.W;
       const T* t = xs + q * g.xstride + (rbi * R * S) * g.pitch + cbi * V * S + g.cshift;
 #pragma unroll
       for (int uu = 0; uu < U; ++uu) {
         if (!row_used<K, D, R, S>(uu)) continue;
         float win[W4];
+        if (xd) {
+          const int iy = iyb + uu;
+          if ((unsigned)iy >= (unsigned)c.H) continue;
 #pragma unroll
-        for (int i = 0; i < W4 / 4; ++i) ld4<T>(t + uu * g.pitch + 4 * i, win + 4 * i);
+          for (int i = 0; i < WN; ++i) win[DL + i] = cin[i] ? ld1<T>(xp + iy * c.W + ixb + i) : 0.f;
+        } else {
+#pragma unroll
+          for (int i = 0; i < W4 / 4; ++i) ld4<T>(t + uu * g.pitch + 4 * i, win + 4 * i);
+        }
 #pragma unroll
         for (int r = 0; r < R; ++r)
 #pragma unroll
@@ -306,6 +360,25 @@ cudaError_t run_wgrad_t(const Conv& c, const void* x, const void* gy, float* ws,
     g.goff = g.ppc * g.xstride;
   }
   g.stage_elems = stage_round((int64_t)g.goff + (int64_t)g.ppc * g.gstride, ES);
+  // dense staging of whole planes whose rows are not 16-byte multiples
+  if (!g.tma && g.nbands == 1) {
+    if ((g.xmode == kCopy4 || g.xmode == kCopySync) && (reinterpret_cast<uintptr_t>(x) % 16) == 0)
+      g.xmode = kCopyDense;
+    if ((g.gmode == kCopy4 || g.gmode == kCopySync) && (reinterpret_cast<uintptr_t>(gy) % 16) == 0)
+      g.gmode = kCopyDense;
+  }
+  if (g.xmode == kCopyDense || g.gmode == kCopyDense) {
+    // a dense tensor is read in place from its staging segments
+    if (g.xmode == kCopyDense) g.xstride = 0;
+    if (g.gmode == kCopyDense) g.gstride = 0;
+    g.goff = round_up((int64_t)g.ppc * g.xstride, A128);
+    g.stage_elems = stage_round((int64_t)g.goff + (int64_t)g.ppc * g.gstride, ES);
+    g.xseg = g.xmode == kCopyDense ? dense_seg<T>(c.H * c.W) : 0;
+    g.gseg = g.gmode == kCopyDense ? dense_seg<T>(c.Ho * c.Wo) : 0;
+    g.stg_off = g.stage_elems;
+    g.gstg_off = stage_round((int64_t)g.stg_off + (int64_t)g.ppc * g.xseg, ES);
+    g.stage_elems = stage_round((int64_t)g.gstg_off + (int64_t)g.ppc * M * g.gseg, ES);
+  }
   g.tma_slice_bytes = (uint32_t)((g.x_elems + (int64_t)M * g.g_elems) * ES);
   g.tma_bytes = g.tma_slice_bytes * g.ppc;
   switch (dl) {
