@@ -1,0 +1,56 @@
+// Large-kernel depthwise forward and stride-1 grad-input: shape support and
+// dtype dispatch (kernels in large_impl.cuh, compiled once per storage type).
+#include "plan.h"
+
+namespace dwconv {
+namespace large {
+
+template <typename T>
+cudaError_t fwd_t(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s);
+template <typename T>
+cudaError_t bwd_t(const Conv& c, const void* gy, const void* w, void* gx, bool acc, cudaStream_t s);
+template <typename T>
+cudaError_t wgrad_t(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s);
+
+bool supported(const Conv& c) {
+  // square kernels of the compiled sizes, stride 1, dilation 1, one filter per channel,
+  // planes up to 128 x 128
+  if (c.kh != c.kw) return false;
+  if (c.kh != 7 && c.kh != 9 && c.kh != 11 && c.kh != 13 && c.kh != 15 && c.kh != 21 && c.kh != 27 &&
+      c.kh != 31)
+    return false;
+  if (c.sh != 1 || c.sw != 1 || c.dh != 1 || c.dw != 1 || c.m != 1) return false;
+  if (c.ph != c.pw || c.ph > c.kh - 1) return false;
+  if (c.H > 128 || c.W > 128 || c.Ho > 128 || c.Wo > 128) return false;
+  return true;
+}
+
+cudaError_t fwd(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s) {
+  cudaError_t e = cudaErrorInvalidConfiguration;
+  DWCONV_DISPATCH_DTYPE(c.dtype, T, e = fwd_t<T>(c, x, w, b, y, s));
+  return e;
+}
+
+int wgrad_chunks(const Conv& c) {
+  // several units per resident CTA (about 2 per SM), a bounded chain per thread
+  int64_t chunks = (152 * 2 * 4 + c.C - 1) / c.C;
+  if (chunks > c.N) chunks = c.N;
+  if (chunks < 1) chunks = 1;
+  const int64_t nb = (c.N + chunks - 1) / chunks;
+  return (int)(c.N > 0 ? (c.N + nb - 1) / nb : 1);
+}
+
+cudaError_t wgrad(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s) {
+  cudaError_t e = cudaErrorInvalidConfiguration;
+  DWCONV_DISPATCH_DTYPE(c.dtype, T, e = wgrad_t<T>(c, x, gy, ws, chunks, s));
+  return e;
+}
+
+cudaError_t bwd_data(const Conv& c, const void* gy, const void* w, void* gx, bool acc, cudaStream_t s) {
+  cudaError_t e = cudaErrorInvalidConfiguration;
+  DWCONV_DISPATCH_DTYPE(c.dtype, T, e = bwd_t<T>(c, gy, w, gx, acc, s));
+  return e;
+}
+
+}  // namespace large
+}  // namespace dwconv

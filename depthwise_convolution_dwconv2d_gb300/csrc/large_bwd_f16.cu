@@ -1,0 +1,8 @@
+// Large-kernel stride-1 grad-input for __half storage.
+#include "large_impl.cuh"
+
+namespace dwconv {
+namespace large {
+template cudaError_t bwd_t<__half>(const Conv&, const void*, const void*, void*, bool, cudaStream_t);
+}  // namespace large
+}  // namespace dwconv

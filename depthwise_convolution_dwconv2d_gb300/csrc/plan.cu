@@ -29,17 +29,20 @@ const char* algo_name(Algo a) {
 Algo plan_fwd(const Conv& c) {
   if (force_generic()) return Algo::Generic;
   if (tile::fwd_supported(c)) return Algo::Tile;
+  if (large::supported(c)) return Algo::Large;
   return Algo::Generic;
 }
 
 Algo plan_bwd_data(const Conv& c) {
   if (force_generic()) return Algo::Generic;
   if (c.sh == 1 ? tile::bwd1_supported(c) : tile::bwd2_supported(c)) return Algo::Tile;
+  if (large::supported(c)) return Algo::Large;
   return Algo::Generic;
 }
 
 WPlan plan_bwd_weight(const Conv& c) {
   if (!force_generic() && tile::wgrad_supported(c)) return WPlan{Algo::Tile, tile::wgrad_chunks(c)};
+  if (!force_generic() && large::supported(c)) return WPlan{Algo::Large, large::wgrad_chunks(c)};
   // generic first pass: a chunk of whole samples per block, at most 2^20
   // positions per chunk so each thread's serial chain stays <= 4096 terms.
   const int64_t hw = c.Ho * c.Wo;
@@ -55,6 +58,7 @@ cudaError_t run_fwd(Algo a, const Conv& c, const void* x, const void* w, const v
                     cudaStream_t s) {
   switch (a) {
     case Algo::Tile: return tile::fwd(c, x, w, b, y, s);
+    case Algo::Large: return large::fwd(c, x, w, b, y, s);
     default: return fwd_generic(c, x, w, b, y, s);
   }
 }
@@ -64,6 +68,7 @@ cudaError_t run_bwd_data(Algo a, const Conv& c, const void* gy, const void* w, v
   switch (a) {
     case Algo::Tile:
       return c.sh == 1 ? tile::bwd1(c, gy, w, gx, accumulate, s) : tile::bwd2(c, gy, w, gx, accumulate, s);
+    case Algo::Large: return large::bwd_data(c, gy, w, gx, accumulate, s);
     default: return bwd_data_generic(c, gy, w, gx, accumulate, s);
   }
 }
@@ -74,6 +79,9 @@ cudaError_t run_bwd_weight(const WPlan& p, const Conv& c, const void* x, const v
   switch (p.algo) {
     case Algo::Tile:
       e = tile::wgrad(c, x, gy, ws, p.chunks, s);
+      break;
+    case Algo::Large:
+      e = large::wgrad(c, x, gy, ws, p.chunks, s);
       break;
     default:
       e = bwd_weight_generic_pass1(c, x, gy, ws, p.chunks, gw != nullptr, gb != nullptr, s);

@@ -57,4 +57,13 @@ cudaError_t bwd_multi(int nb, const Conv* cs, const void* gy, const void* const*
 
 Algo plan_multi(int nb, const Conv* cs);
 
+namespace large {
+// large.cu: large-kernel direct convolution (fp32 FMA), stride 1
+bool supported(const Conv& c);
+cudaError_t fwd(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s);
+cudaError_t bwd_data(const Conv& c, const void* gy, const void* w, void* gx, bool acc, cudaStream_t s);
+int wgrad_chunks(const Conv& c);
+cudaError_t wgrad(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s);
+}  // namespace large
+
 }  // namespace dwconv

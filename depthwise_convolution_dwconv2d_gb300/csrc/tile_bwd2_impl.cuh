@@ -125,12 +125,8 @@ bwd2_kernel(Conv c, Bwd2Cfg g, const __grid_constant__ CUtensorMap tmap, unsigne
     const int64_t p0 = (int64_t)grp * g.ppc;
     const int np = (int)((nplanes - p0) < g.ppc ? (nplanes - p0) : g.ppc);
     const int u0 = band * g.thu;  // first u row of the band (gx row S*u0)
-    if (g.mode == kCopyDense) {
-      repitch<T>(cur, np * m, g.tile_elems, g.pitch, (k & 1) ? stg1 : stg0, g.seg,
-                 [&](int s) { return gy_plane(p0, s); }, (int)c.Ho, (int)c.Wo, u0 + g.row0, g.tr, g.trdiv,
-                 g.ix0);
-      __syncthreads();
-    }
+    const T* stg = (k & 1) ? stg1 : stg0;
+    const bool dense = g.mode == kCopyDense;
     const int total = np * (int)g.d_plane.d;
     float wr[K * K];
     int cur_pl = -1;
@@ -157,11 +153,24 @@ bwd2_kernel(Conv c, Bwd2Cfg g, const __grid_constant__ CUtensorMap tmap, unsigne
           cur_pl = pl;
         }
         const T* t = cur + (pl * m + j) * g.tile_elems + (rbi * R) * g.pitch + cbi * V + g.cshift;
+        // dense: grad_out plane coordinates of window (0, 0)
+        const T* dp = dense ? dense_plane(stg, g.seg, pl * m + j, gy_plane(p0, pl * m + j)) : nullptr;
+        const int gyr = u0 + g.row0 + rbi * R, gyc = g.ix0 + g.cshift + DL + cbi * V;
 #pragma unroll
         for (int ut = 0; ut < R + SP; ++ut) {
           float win[W4];
+          if (dense) {
+            const int iy = gyr + ut;
+            if ((unsigned)iy >= (unsigned)c.Ho) continue;
 #pragma unroll
-          for (int i = 0; i < W4 / 4; ++i) ld4<T>(t + ut * g.pitch + 4 * i, win + 4 * i);
+            for (int i = 0; i < V + SP; ++i) {
+              const int ix = gyc + i;
+              win[DL + i] = (unsigned)ix < (unsigned)c.Wo ? ld1<T>(dp + iy * c.Wo + ix) : 0.f;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < W4 / 4; ++i) ld4<T>(t + ut * g.pitch + 4 * i, win + 4 * i);
+          }
 #pragma unroll
           for (int r = 0; r < R; ++r)
 #pragma unroll
@@ -277,7 +286,7 @@ cudaError_t run_bwd2_t(const Conv& c, const void* gy, const void* w, void* gx, b
   if ((g.mode == kCopy4 || g.mode == kCopySync) && g.nbands == 1 &&
       (reinterpret_cast<uintptr_t>(gy) % 16) == 0) {
     const int seg = dense_seg<T>(c.Ho * c.Wo);
-    const int64_t per = ((int64_t)g.tile_elems + seg) * ES * c.m;
+    const int64_t per = (int64_t)seg * ES * c.m;  // dense planes are read in place
     int64_t dppc = (2 * kNT + items - 1) / items;
     if (dppc > target / per) dppc = target / per;
     if (dppc >= 1) {
@@ -295,7 +304,7 @@ cudaError_t run_bwd2_t(const Conv& c, const void* gy, const void* w, void* gx, b
   if (tma) g.mode = kCopyTMA;
   g.ppc = (int)ppc;
   g.groups = (nplanes + ppc - 1) / ppc;
-  g.stage_elems = stage_round((int64_t)g.ppc * c.m * g.tile_elems, ES);
+  g.stage_elems = g.mode == kCopyDense ? 0 : stage_round((int64_t)g.ppc * c.m * g.tile_elems, ES);
   g.tma_bytes = (uint32_t)((int64_t)g.ppc * c.m * g.tile_elems * ES);
   g.stg_elems = g.mode == kCopyDense ? stage_round((int64_t)g.ppc * c.m * g.seg, ES) : 0;
   g.vec_out = (reinterpret_cast<uintptr_t>(gx) % (4 * ES) == 0) && c.W % 4 == 0;

@@ -1,9 +1,8 @@
-// Forward and stride-1 grad-input tile kernels for __nv_bfloat16 storage.
+// Forward tile kernels for __nv_bfloat16 storage.
 #include "tile_fwd_impl.cuh"
 
 namespace dwconv {
 namespace tile {
 template cudaError_t fwd_t<__nv_bfloat16>(const Conv&, const void*, const void*, const void*, void*, cudaStream_t);
-template cudaError_t bwd1_t<__nv_bfloat16>(const Conv&, const void*, const void*, void*, bool, cudaStream_t);
 }  // namespace tile
 }  // namespace dwconv

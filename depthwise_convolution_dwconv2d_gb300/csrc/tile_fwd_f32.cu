@@ -1,9 +1,8 @@
-// Forward and stride-1 grad-input tile kernels for float storage.
+// Forward tile kernels for float storage.
 #include "tile_fwd_impl.cuh"
 
 namespace dwconv {
 namespace tile {
 template cudaError_t fwd_t<float>(const Conv&, const void*, const void*, const void*, void*, cudaStream_t);
-template cudaError_t bwd1_t<float>(const Conv&, const void*, const void*, void*, bool, cudaStream_t);
 }  // namespace tile
 }  // namespace dwconv

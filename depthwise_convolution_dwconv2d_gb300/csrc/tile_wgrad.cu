@@ -23,8 +23,8 @@
 namespace dwconv {
 namespace tile {
 
-template <typename T>
-cudaError_t wgrad_t(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s);
+template <typename T, int MSEL>
+cudaError_t wgrad_sel_t(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s);
 
 bool wgrad_supported(const Conv& c) {
   if (c.kh != c.kw || c.sh != c.sw || c.dh != c.dw || c.W > 1024 || c.Wo > 1024) return false;
@@ -50,7 +50,11 @@ int wgrad_chunks(const Conv& c) {
 
 cudaError_t wgrad(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s) {
   cudaError_t e = cudaErrorInvalidConfiguration;
-  DWCONV_DISPATCH_DTYPE(c.dtype, T, e = wgrad_t<T>(c, x, gy, ws, chunks, s));
+  if (c.m == 1) {
+    DWCONV_DISPATCH_DTYPE(c.dtype, T, e = (wgrad_sel_t<T, 1>(c, x, gy, ws, chunks, s)));
+  } else {
+    DWCONV_DISPATCH_DTYPE(c.dtype, T, e = (wgrad_sel_t<T, 2>(c, x, gy, ws, chunks, s)));
+  }
   return e;
 }
 

@@ -1,0 +1,8 @@
+// Weight-gradient tile kernels (multiplier 2) for __half storage.
+#include "tile_wgrad_impl.cuh"
+
+namespace dwconv {
+namespace tile {
+template cudaError_t wgrad_sel_t<__half, 2>(const Conv&, const void*, const void*, float*, int, cudaStream_t);
+}  // namespace tile
+}  // namespace dwconv

@@ -1,8 +1,8 @@
-// wgrad tile kernels for __half storage.
+// Weight-gradient tile kernels (multiplier 1) for __half storage.
 #include "tile_wgrad_impl.cuh"
 
 namespace dwconv {
 namespace tile {
-template cudaError_t wgrad_t<__half>(const Conv&, const void*, const void*, float*, int, cudaStream_t);
+template cudaError_t wgrad_sel_t<__half, 1>(const Conv&, const void*, const void*, float*, int, cudaStream_t);
 }  // namespace tile
 }  // namespace dwconv

@@ -391,10 +391,14 @@ cudaError_t run_wgrad_t(const Conv& c, const void* x, const void* gy, float* ws,
 
 }  // namespace
 
-template <typename T>
-cudaError_t wgrad_t(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s) {
-#define X(K, S, D, M) \
-  if (c.kh == K && c.sh == S && c.dh == D && c.m == M) return run_wgrad_t<T, K, S, D, M>(c, x, gy, ws, chunks, s);
+// Dispatch over the compiled cases with multiplier MSEL only (each
+// multiplier's kernels are compiled in their own translation unit).
+template <typename T, int MSEL>
+cudaError_t wgrad_sel_t(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s) {
+#define X(K, S, D, M)                                                                      \
+  if constexpr (M == MSEL) {                                                                \
+    if (c.kh == K && c.sh == S && c.dh == D && c.m == M) return run_wgrad_t<T, K, S, D, M>(c, x, gy, ws, chunks, s); \
+  }
   DW_WGRAD_CASES(X)
 #undef X
   return cudaErrorInvalidConfiguration;

@@ -331,3 +331,14 @@ def test_generic_and_planned_kernels_agree():
 def test_no_bounded_wait_gave_up():
     """Every tile copy the suite waited for arrived (no timeouts counted)."""
     assert B.dwconv_device_timeouts() == 0
+
+
+@pytest.mark.parametrize("L", [WL.Layer(N=3, C=5, H=21, W=19, k=7, p=3, bias=True, dtype="f32"),
+                               WL.Layer(N=2, C=3, H=30, W=33, k=13, p=6, dtype="bf16"),
+                               WL.Layer(N=3, C=7, H=17, W=16, k=31, p=15, bias=True, dtype="f16"),
+                               WL.Layer(N=2, C=6, H=12, W=12, k=9, p=2, dtype="f32")],
+                         ids=["k7f32", "k13bf16", "k31f16", "k9p2"])
+def test_large_kernels_planes_straddle_samples(L):
+    """Large kernels where a CTA's planes span two samples (C not a multiple
+    of the planes per CTA), with bias and non-"same" padding."""
+    check_full(L, WL.make_inputs(L), L.label())
