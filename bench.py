@@ -265,6 +265,9 @@ def gpu_arm(args, rank, world):
         items = [i for i in items if i.label() in keep]
         if not items:
             raise SystemExit(f"--layers matched nothing in {args.workload}")
+    if args.batch:
+        # smaller batch of the same layers (profiling runs only)
+        items = [type(i)(**{**i.__dict__, "N": args.batch}) for i in items]
     dist = None
     if world > 1:
         import torch.distributed as dist_
@@ -444,6 +447,8 @@ def gpu_arm(args, rank, world):
         "dtype": sorted({getattr(i, "dtype", "f32") for i in items})[0] if len(items) else "f32",
         "data": "synthetic (SplitMix64 + Box-Muller, seed 0)",
         "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload,
+                   **({"layers": args.layers} if args.layers else {}),
+                   **({"batch_override": args.batch} if args.batch else {}),
                    "parallelism": f"replicas x{world} (no collective)",
                    "l2": "flushed (2x L2 write) before every call; inputs resident in HBM",
                    "step_bytes": step_bytes, "step_fma_valid": step_fma,
@@ -486,6 +491,7 @@ def main():
     ap.add_argument("--fma-probe", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--layers", default="", help="comma-separated layer labels to keep (profiling runs)")
+    ap.add_argument("--batch", type=int, default=0, help="override the batch size (profiling runs)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))

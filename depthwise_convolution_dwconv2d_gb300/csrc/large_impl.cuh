@@ -58,10 +58,13 @@ __device__ __forceinline__ void stage(float* dst, const LCfg& g, int np, SrcOf s
       dst[p * g.tile_elems + q] = (iy >= 0 && iy < Hin && ix >= 0 && ix < Win) ? ld(src_of(p) + (int64_t)iy * Win + ix) : 0.f;
     }
   }
-  for (int e = threadIdx.x; e < np * K * K; e += kNT) {
-    const int p = e / (K * K), t = e - p * (K * K);
+  constexpr int KP = (K + 3) / 4 * 4;  // filter rows padded for 16-byte loads
+  for (int e = threadIdx.x; e < np * K * KP; e += kNT) {
+    const int p = e / (K * KP), t = e - p * (K * KP);
+    const int a = t / KP, b = t - a * KP;
     const int64_t ch = (p0 + p) % C;  // the unit's planes may span two samples
-    dst[p * g.tile_elems + g.wofs + t] = ld(w + ch * (K * K) + (FLIP ? K * K - 1 - t : t));
+    dst[p * g.tile_elems + g.wofs + t] =
+        b < K ? ld(w + ch * (K * K) + (FLIP ? K * K - 1 - (a * K + b) : a * K + b)) : 0.f;
   }
 }
 
@@ -73,7 +76,6 @@ large_kernel(Conv c, LCfg g, const T* __restrict__ in, const T* __restrict__ w, 
   constexpr int WN = V + K - 1;
   constexpr int W4 = (WN + 3) / 4 * 4;
   float* const buf0 = reinterpret_cast<float*>(smraw);
-  float* const buf1 = buf0 + g.ppc * g.tile_elems;
   // stencil geometry: the forward reads x (H x W) and writes y (Ho x Wo);
   // the grad-input reads grad_out (Ho x Wo) and writes gx (H x W)
   const int Hin = FLIP ? (int)c.Ho : (int)c.H, Win = FLIP ? (int)c.Wo : (int)c.W;
@@ -93,23 +95,26 @@ large_kernel(Conv c, LCfg g, const T* __restrict__ in, const T* __restrict__ w, 
     const int np = (int)((nplanes - p0) < g.ppc ? (nplanes - p0) : g.ppc);
     stage<T, K, FLIP>(dst, g, np, [&](int p) { return src_of(p0 + p); }, w, p0, c.C, Hin, Win);
   };
-  int64_t u = blockIdx.x;
-  if (u < units) issue(u, buf0);
-  tile::cp_async_commit();
-  for (int k = 0; u < units; ++k, u += gridDim.x) {
-    const float* cur = (k & 1) ? buf1 : buf0;
-    if (u + gridDim.x < units) issue(u + gridDim.x, (k & 1) ? buf0 : buf1);
+  // one stage: the compute of a unit is long next to its load, and the
+  // other CTAs resident on the SM keep it busy while this one loads
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    issue(u, buf0);
     tile::cp_async_commit();
-    tile::cp_async_wait<1>();
+    tile::cp_async_wait<0>();
     __syncthreads();
+    const float* cur = buf0;
     const int64_t p0 = u * g.ppc;
     const int np = (int)((nplanes - p0) < g.ppc ? (nplanes - p0) : g.ppc);
     const int ipp = (int)g.d_item.d;
+    // items ordered (row block, plane, column block): a warp's lanes share
+    // output rows, so they walk the same kernel rows
+    const int per_rb = np * g.cb;
     for (int it = threadIdx.x; it < np * ipp; it += kNT) {
-      uint32_t pl_, rbi_;
-      const uint32_t rem = g.d_item.divmod((uint32_t)it, pl_);
-      const int cbi = (int)g.d_cb.divmod(rem, rbi_);
-      const int pl = (int)pl_, rbi = (int)rbi_;
+      const int rbi = it / per_rb;
+      const int rem = it - rbi * per_rb;
+      uint32_t pl_;
+      const int cbi = (int)g.d_cb.divmod((uint32_t)rem, pl_);
+      const int pl = (int)pl_;
       const float* t = cur + pl * g.tile_elems;
       const float* wt = t + g.wofs;
       const int oh0 = rbi * R, ow0 = cbi * V;
@@ -124,10 +129,14 @@ large_kernel(Conv c, LCfg g, const T* __restrict__ in, const T* __restrict__ w, 
       if (a_lo < 0) a_lo = 0;
       int a_hi = Hin + g.pad - oh0;
       if (a_hi > K) a_hi = K;
+      constexpr int KP = (K + 3) / 4 * 4;
       for (int a = a_lo; a < a_hi; ++a) {
-        float wrow[K];
+        float wrow[KP];
 #pragma unroll
-        for (int b = 0; b < K; ++b) wrow[b] = wt[a * K + b];
+        for (int b = 0; b < KP / 4; ++b) {
+          const float4 f = *reinterpret_cast<const float4*>(wt + a * KP + 4 * b);
+          wrow[4 * b] = f.x; wrow[4 * b + 1] = f.y; wrow[4 * b + 2] = f.z; wrow[4 * b + 3] = f.w;
+        }
 #pragma unroll
         for (int r = 0; r < R; ++r) {
           const int iy = oh0 + r + a - g.pad;  // input row
@@ -164,10 +173,10 @@ large_kernel(Conv c, LCfg g, const T* __restrict__ in, const T* __restrict__ w, 
   }
 }
 
-template <typename T, int K, bool FLIP>
-cudaError_t run(const Conv& c, const void* in, const void* w, const void* bias, void* out, bool acc,
-                cudaStream_t s) {
-  constexpr int R = 4, V = 4;
+template <typename T, int K, bool FLIP, int R>
+cudaError_t run_r(const Conv& c, const void* in, const void* w, const void* bias, void* out, bool acc,
+                  cudaStream_t s) {
+  constexpr int V = 4;
   constexpr int W4 = (V + K - 1 + 3) / 4 * 4;
   const int Win = FLIP ? (int)c.Wo : (int)c.W;
   const int Hout = FLIP ? (int)c.H : (int)c.Ho, Wout = FLIP ? (int)c.W : (int)c.Wo;
@@ -179,14 +188,14 @@ cudaError_t run(const Conv& c, const void* in, const void* w, const void* bias, 
   if (g.pitch < Win + g.pad) g.pitch = tile::round_up(Win + g.pad, 4);
   g.tr = g.rb * R + K - 1;  // rows read by every block, padded ones included
   g.wofs = tile::round_up((int64_t)g.tr * g.pitch, 4);
-  g.tile_elems = tile::round_up(g.wofs + K * K, 4);
+  g.tile_elems = tile::round_up(g.wofs + K * ((K + 3) / 4 * 4), 4);
   const int64_t plane_bytes = (int64_t)g.tile_elems * 4;
   const int64_t ipp = (int64_t)g.rb * g.cb;
   int64_t ppc = (kNT + ipp - 1) / ipp;
-  const int64_t cap = (96 * 1024) / plane_bytes;
+  const int64_t cap = (72 * 1024) / plane_bytes;
   if (ppc > cap) ppc = cap;
   if (ppc < 1) ppc = 1;
-  if (2 * ppc * plane_bytes > 200 * 1024) return cudaErrorInvalidConfiguration;
+  if (ppc * plane_bytes > 200 * 1024) return cudaErrorInvalidConfiguration;
   g.ppc = (int)ppc;
   const int64_t nplanes = c.N * c.C;
   g.groups = (nplanes + ppc - 1) / ppc;
@@ -195,7 +204,7 @@ cudaError_t run(const Conv& c, const void* in, const void* w, const void* bias, 
   g.d_item = FastDiv((uint32_t)ipp);
   g.d_cb = FastDiv((uint32_t)g.cb);
   auto kern = large_kernel<T, K, R, V, FLIP>;
-  const size_t smem = 2 * (size_t)g.ppc * g.tile_elems * 4;
+  const size_t smem = (size_t)g.ppc * g.tile_elems * 4;
   cudaError_t e = tile::set_smem(kern, smem);
   if (e != cudaSuccess) return e;
   const int grid = tile::persistent_grid(kern, smem, g.groups);
@@ -298,6 +307,7 @@ large_wgrad_kernel(Conv c, WLCfg g, const T* __restrict__ x, const T* __restrict
             const int a = a0 + r;
             // x tile row of input row oh + a - pad is oh + a (origin -pad)
             if (a >= K) break;
+            if ((unsigned)(oh + a - g.pad) >= (unsigned)H) continue;  // a padding row: zero
             const float* xrow = xs + (oh + a) * g.xpitch + b0;
             float xw[V + 3 + 4];
             {
@@ -360,6 +370,16 @@ large_wgrad_kernel(Conv c, WLCfg g, const T* __restrict__ x, const T* __restrict
     u = un;
     sidx = sn;
   }
+}
+
+// Two output rows per thread on planes of up to 32 rows (more blocks, so one
+// or two planes fill a CTA), four on larger planes.
+template <typename T, int K, bool FLIP>
+cudaError_t run(const Conv& c, const void* in, const void* w, const void* bias, void* out, bool acc,
+                cudaStream_t s) {
+  const int64_t Hout = FLIP ? c.H : c.Ho;
+  if (Hout <= 32) return run_r<T, K, FLIP, 2>(c, in, w, bias, out, acc, s);
+  return run_r<T, K, FLIP, 4>(c, in, w, bias, out, acc, s);
 }
 
 template <typename T, int K>
