@@ -15,6 +15,13 @@ bool force_generic() {
   return e && std::strcmp(e, "generic") == 0;
 }
 
+// DWCONV_FORCE_ALGO=direct keeps the large 16-bit shapes on the direct
+// kernels (used by the tests to cross-check the tensor-core ones).
+bool allow_ibgemm() {
+  const char* e = std::getenv("DWCONV_FORCE_ALGO");
+  return !(e && (std::strcmp(e, "generic") == 0 || std::strcmp(e, "direct") == 0));
+}
+
 }  // namespace
 
 const char* algo_name(Algo a) {
@@ -22,6 +29,7 @@ const char* algo_name(Algo a) {
     case Algo::Generic: return "generic";
     case Algo::Tile: return "tile";
     case Algo::Large: return "large";
+    case Algo::IBGemm: return "ibgemm";
   }
   return "unknown";
 }
@@ -29,6 +37,7 @@ const char* algo_name(Algo a) {
 Algo plan_fwd(const Conv& c) {
   if (force_generic()) return Algo::Generic;
   if (tile::fwd_supported(c)) return Algo::Tile;
+  if (allow_ibgemm() && ibg::fwd_supported(c)) return Algo::IBGemm;
   if (large::supported(c)) return Algo::Large;
   return Algo::Generic;
 }
@@ -36,6 +45,7 @@ Algo plan_fwd(const Conv& c) {
 Algo plan_bwd_data(const Conv& c) {
   if (force_generic()) return Algo::Generic;
   if (c.sh == 1 ? tile::bwd1_supported(c) : tile::bwd2_supported(c)) return Algo::Tile;
+  if (allow_ibgemm() && ibg::bwd_data_supported(c)) return Algo::IBGemm;
   if (large::supported(c)) return Algo::Large;
   return Algo::Generic;
 }
@@ -59,6 +69,12 @@ cudaError_t run_fwd(Algo a, const Conv& c, const void* x, const void* w, const v
   switch (a) {
     case Algo::Tile: return tile::fwd(c, x, w, b, y, s);
     case Algo::Large: return large::fwd(c, x, w, b, y, s);
+    case Algo::IBGemm: {
+      // a misaligned pointer rules the tensor-core kernel out for this call only
+      const cudaError_t e = ibg::fwd(c, x, w, b, y, s);
+      if (e != cudaErrorNotSupported) return e;
+      return large::supported(c) ? large::fwd(c, x, w, b, y, s) : fwd_generic(c, x, w, b, y, s);
+    }
     default: return fwd_generic(c, x, w, b, y, s);
   }
 }
@@ -69,6 +85,12 @@ cudaError_t run_bwd_data(Algo a, const Conv& c, const void* gy, const void* w, v
     case Algo::Tile:
       return c.sh == 1 ? tile::bwd1(c, gy, w, gx, accumulate, s) : tile::bwd2(c, gy, w, gx, accumulate, s);
     case Algo::Large: return large::bwd_data(c, gy, w, gx, accumulate, s);
+    case Algo::IBGemm: {
+      const cudaError_t e = ibg::bwd_data(c, gy, w, gx, accumulate, s);
+      if (e != cudaErrorNotSupported) return e;
+      return large::supported(c) ? large::bwd_data(c, gy, w, gx, accumulate, s)
+                                 : bwd_data_generic(c, gy, w, gx, accumulate, s);
+    }
     default: return bwd_data_generic(c, gy, w, gx, accumulate, s);
   }
 }

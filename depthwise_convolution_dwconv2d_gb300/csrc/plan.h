@@ -11,6 +11,7 @@ enum class Algo {
   Generic = 0,   // generic.cu: any shape
   Tile = 1,      // tile_fwd.cu / tile_bwd.cu: register-blocked smem tiles, small kernels
   Large = 2,     // large.cu: large-kernel direct convolution
+  IBGemm = 3,    // ibgemm.cu: large-kernel implicit batched GEMM on tcgen05 (fp16 / bf16)
 };
 
 struct WPlan {
@@ -65,5 +66,14 @@ cudaError_t bwd_data(const Conv& c, const void* gy, const void* w, void* gx, boo
 int wgrad_chunks(const Conv& c);
 cudaError_t wgrad(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s);
 }  // namespace large
+
+namespace ibg {
+// ibgemm.cu: tensor-core implicit batched GEMM, stride 1, 16-bit data
+bool fwd_supported(const Conv& c);
+bool bwd_data_supported(const Conv& c);
+// cudaErrorNotSupported when this call's input pointer is not 16-byte aligned
+cudaError_t fwd(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s);
+cudaError_t bwd_data(const Conv& c, const void* gy, const void* w, void* gx, bool acc, cudaStream_t s);
+}  // namespace ibg
 
 }  // namespace dwconv

@@ -68,6 +68,21 @@ bool encode_4d(CUtensorMap* map, const void* base, int dtype, uint64_t cols, uin
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_3d_sw128(CUtensorMap* map, const void* base, int dtype, uint64_t cols, uint64_t rows,
+                     uint64_t planes, uint32_t box_cols, uint32_t box_rows, uint32_t box_planes) {
+  EncodeFn fn = encode_fn();
+  if (!fn || dtype == DWCONV_F32 || box_cols * 2 != 128) return false;
+  const CUtensorMapDataType dt =
+      dtype == DWCONV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const cuuint64_t dims[3] = {cols, rows, planes};
+  const cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
+  const cuuint32_t box[3] = {box_cols, box_rows, box_planes};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 unsigned int* timeout_counter() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;

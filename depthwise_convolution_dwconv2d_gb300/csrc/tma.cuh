@@ -94,6 +94,12 @@ bool encode_3d(CUtensorMap* map, const void* base, int dtype, uint64_t cols, uin
 bool encode_4d(CUtensorMap* map, const void* base, int dtype, uint64_t cols, uint64_t rows, uint64_t d2,
                uint64_t d3, uint32_t box_cols, uint32_t box_rows, uint32_t box_d2, uint32_t box_d3);
 
+// Host: 3-D tiled tensor map over a row-major [planes][rows][cols] 16-bit
+// tensor with the 128-byte swizzle (box_cols * 2 must be 128): the layout the
+// tensor-core operand descriptors read as K-major with 128-byte swizzle.
+bool encode_3d_sw128(CUtensorMap* map, const void* base, int dtype, uint64_t cols, uint64_t rows,
+                     uint64_t planes, uint32_t box_cols, uint32_t box_rows, uint32_t box_planes);
+
 // Host: device address of the timeout counter on the current device (looked
 // up once per device), or nullptr if the lookup failed.
 unsigned int* timeout_counter();

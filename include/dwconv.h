@@ -172,8 +172,12 @@ dwconv_status_t dwconv2d_bwd_data_multi(int nbranch, const dwconv2d_desc_t* desc
 const char* dwconv_status_string(dwconv_status_t status);
 
 /* Name of the kernel family the planner picks for a pass (0 = fwd,
- * 1 = bwd_data, 2 = bwd_weight) of this descriptor, or "invalid". Host only;
- * for logs and tests. */
+ * 1 = bwd_data, 2 = bwd_weight) of this descriptor: "tile" (small filters),
+ * "large" (large-filter direct convolution), "ibgemm" (large-filter fp16 /
+ * bf16 forward and grad-input as an implicit batched GEMM on the tensor
+ * cores), "generic" (any shape) or "invalid". Host only; for logs and tests.
+ * An "ibgemm" pass whose input pointer is not 16-byte aligned runs on the
+ * direct kernels instead. */
 const char* dwconv2d_plan_name(const dwconv2d_desc_t* desc, int pass);
 
 /* Kernel family used by dwconv2d_fwd_multi / dwconv2d_bwd_data_multi for

@@ -342,3 +342,64 @@ def test_large_kernels_planes_straddle_samples(L):
     """Large kernels where a CTA's planes span two samples (C not a multiple
     of the planes per CTA), with bias and non-"same" padding."""
     check_full(L, WL.make_inputs(L), L.label())
+
+
+# ------------------------------------------------ tensor-core large kernels
+IBG_CASES = [
+    WL.Layer(N=3, C=5, H=32, W=32, k=31, p=15, bias=True, dtype="f16"),
+    WL.Layer(N=20, C=3, H=48, W=48, k=13, p=6, dtype="bf16"),
+    WL.Layer(N=2, C=4, H=17, W=16, k=9, p=4, bias=True, dtype="f16"),
+    WL.Layer(N=2, C=3, H=24, W=24, k=11, p=2, dtype="bf16"),
+    WL.Layer(N=130, C=2, H=16, W=16, k=15, p=7, dtype="bf16"),
+    WL.Layer(N=1, C=3, H=64, W=64, k=27, p=13, dtype="f16"),
+]
+IBG_IDS = ["k31f16_T8", "k13bf16_W48", "k9f16_raggedM", "k11bf16_p2", "k15bf16_N130", "k27f16_W64"]
+
+
+@pytest.mark.parametrize("L", IBG_CASES, ids=IBG_IDS)
+def test_ibgemm_vs_oracle(L):
+    """Implicit batched GEMM on the tensor cores: several M tiles per plane, a
+    ragged last tile, K steps that straddle input rows (W = 48), a ragged batch
+    (zero-filled samples), non-"same" padding and a batch above 128."""
+    d = desc_of(L)
+    assert B.dwconv2d_plan_name(d, 0) == "ibgemm"
+    if L.p == L.k // 2:
+        assert B.dwconv2d_plan_name(d, 1) == "ibgemm"
+    check_full(L, WL.make_inputs(L), L.label())
+
+
+@pytest.mark.parametrize("L", [IBG_CASES[0], IBG_CASES[1]], ids=IBG_IDS[:2])
+def test_ibgemm_and_direct_agree(L):
+    """The tensor-core kernels and the direct large-kernel ones agree."""
+    inp = WL.make_inputs(L)
+    a = run_all(L, inp)
+    os.environ["DWCONV_FORCE_ALGO"] = "direct"
+    try:
+        assert B.dwconv2d_plan_name(desc_of(L), 0) == "large"
+        b = run_all(L, inp)
+    finally:
+        del os.environ["DWCONV_FORCE_ALGO"]
+    for u, v in zip(a[:2], b[:2]):
+        assert_close(u, v, L.dtype, L.k * L.k, "ibgemm vs direct")
+
+
+def test_ibgemm_misaligned_input_falls_back():
+    """An input pointer off the 16-byte grid runs on the direct kernels."""
+    th = torch()
+    L = IBG_CASES[2]
+    inp = WL.make_inputs(L)
+    d = desc_of(L)
+    n = L.N * L.C * L.H * L.W
+    xbuf = empty_dev((n + 8,), L.dtype)
+    xv = xbuf[1:1 + n].view(L.N, L.C, L.H, L.W)
+    xv.copy_(to_dev(inp.x))
+    w, b = to_dev(inp.w), to_dev(inp.b)
+    y = empty_dev((L.N, L.C, L.Ho, L.Wo), L.dtype)
+    B.dwconv2d_fwd(d, xv, w, b, y)
+    th.cuda.synchronize()
+    assert_close(to_f64(y), oracle.fwd(oconv(L), inp.x.f64, inp.w.f64, inp.b.f64), L.dtype, L.k * L.k,
+                 "misaligned fwd")
+
+
+def test_no_bounded_wait_gave_up_after_ibgemm():
+    assert B.dwconv_device_timeouts() == 0
