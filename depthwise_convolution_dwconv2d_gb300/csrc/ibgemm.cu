@@ -139,6 +139,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
   asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
 
+// One lane of the (converged) warp; the others get false.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n .reg .b32 r;\n .reg .pred p;\n elect.sync r|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // Named barrier over the builder warps.
 __device__ __forceinline__ void builders_sync() {
   asm volatile("bar.sync 1, %0;\n" ::"n"(kBuilders) : "memory");
@@ -177,6 +186,22 @@ __host__ __device__ __forceinline__ void k_range(const ICfg& g, int t, int& kc_l
   kc_hi = ((ih_hi + 1) * g.Wi + kKs - 1) / kKs;
 }
 
+// Walk over this CTA's units u0..u1-1 as (channel c, tile t) without a
+// division per unit.
+struct Units {
+  int64_t c, u, u1;
+  int t, T;
+  __device__ __forceinline__ Units(int64_t u0_, int64_t u1_, int T_) : u(u0_), u1(u1_), T(T_) {
+    c = u0_ / T_;
+    t = (int)(u0_ - c * T_);
+  }
+  __device__ __forceinline__ bool more() const { return u < u1; }
+  __device__ __forceinline__ void next() {
+    ++u;
+    if (++t == T) { t = 0; ++c; }
+  }
+};
+
 // Stage ring position: stage index and the parity of its current use.
 struct Ring {
   int s = 0;
@@ -189,7 +214,7 @@ struct Ring {
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 2)
-ibgemm_kernel(ICfg g, const __grid_constant__ CUtensorMap xmap, unsigned int* timeouts, const T* __restrict__ w,
+ibgemm_kernel(ICfg g, const __grid_constant__ CUtensorMap xmap, unsigned int* timeouts, const T* __restrict__ w_,
               const T* __restrict__ bias, T* __restrict__ y, int accumulate_out) {
   extern __shared__ __align__(1024) unsigned char smdyn[];
   // fullB[s]: the producer's expect_tx arrival and the copy's bytes; afull[s]:
@@ -235,11 +260,10 @@ ibgemm_kernel(ICfg g, const __grid_constant__ CUtensorMap xmap, unsigned int* ti
     if (lane == 0) {
       Ring r;
       uint32_t issued = 0;
-      for (int64_t u = u0; u < u1; ++u) {
-        const int64_t c = u / g.T;
-        const int t = (int)(u - c * g.T);
+      for (Units w(u0, u1, g.T); w.more(); w.next()) {
+        const int64_t c = w.c;
         int kc_lo, kc_hi;
-        k_range(g, t, kc_lo, kc_hi);
+        k_range(g, w.t, kc_lo, kc_hi);
         for (int kc = kc_lo; kc < kc_hi && !*abortp; ++kc, r.next()) {
           if (r.wrapped && !wait_bar(&freeS[r.s], r.ph ^ 1, timeouts, abortp, kSleepNs)) { *abortp = 1; break; }
           tma::mbar_expect_tx(&fullB[r.s], sbytes);
@@ -257,37 +281,35 @@ ibgemm_kernel(ICfg g, const __grid_constant__ CUtensorMap xmap, unsigned int* ti
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    // ---- MMA issuer --------------------------------------------------------
-    if (lane == 0) {
-      Ring r;
-      uint32_t tiles = 0;
-      const uint64_t bdesc0 = smem_desc(tma::smem_u32(B));
-      const uint32_t bstep = g.bbytes >> 4;  // descriptor start-address units per B atom
-      for (int64_t u = u0; u < u1; ++u, ++tiles) {
-        const int64_t c = u / g.T;
-        const int t = (int)(u - c * g.T);
-        int kc_lo, kc_hi;
-        k_range(g, t, kc_lo, kc_hi);
-        const int ab = tiles & (g.nacc - 1);
-        const uint32_t ause = g.nacc == 2 ? tiles >> 1 : tiles;
-        // the epilogue must have drained this accumulator
-        if (ause > 0 && !wait_bar(&accfree[ab], (ause - 1) & 1, timeouts, abortp)) *abortp = 1;
+    // ---- MMA issuer: the whole warp walks the loop (so descriptors stay in
+    // uniform registers) and one elected lane issues each instruction ------
+    Ring r;
+    uint32_t tiles = 0;
+    bool polled = false;  // the current ring position is known to be ready
+    const uint64_t bdesc0 = smem_desc(tma::smem_u32(B));
+    const uint32_t bstep = g.bbytes >> 4;  // descriptor start-address units per B atom
+    for (Units w(u0, u1, g.T); w.more(); w.next(), ++tiles) {
+      int kc_lo, kc_hi;
+      k_range(g, w.t, kc_lo, kc_hi);
+      const int ab = tiles & (g.nacc - 1);
+      const uint32_t ause = g.nacc == 2 ? tiles >> 1 : tiles;
+      // the epilogue must have drained this accumulator
+      bool okf = ause == 0 || wait_bar(&accfree[ab], (ause - 1) & 1, timeouts, abortp);
+      if (!__all_sync(0xffffffffu, okf)) *abortp = 1;
+      tc_fence_after();
+      const uint32_t dt = tmem + ab * g.acc_cols;
+      for (int kc = kc_lo; kc < kc_hi; ++kc, r.next()) {
+        // the stage's copy and block were polled right after the previous
+        // step's MMAs went out; wait only if one of them was not complete
+        bool ok = true;
+        if (!polled)
+          ok = !*abortp && wait_bar(&fullB[r.s], r.ph, timeouts, abortp) &&
+               wait_bar(&afull[r.s], r.ph, timeouts, abortp);
+        if (!__all_sync(0xffffffffu, ok)) { *abortp = 1; polled = false; continue; }
         tc_fence_after();
-        const uint32_t dt = tmem + ab * g.acc_cols;
-        for (int kc = kc_lo; kc < kc_hi; ++kc, r.next()) {
-          // both polls go out back to back so their latencies overlap
-          const bool rb = tma::mbar_try_wait(&fullB[r.s], r.ph);
-          const bool ra = tma::mbar_try_wait(&afull[r.s], r.ph);
-          if (!(rb && ra)) {
-            if (*abortp || !wait_bar(&fullB[r.s], r.ph, timeouts, abortp) ||
-                !wait_bar(&afull[r.s], r.ph, timeouts, abortp)) {
-              *abortp = 1;
-              continue;
-            }
-          }
-          tc_fence_after();
-          const uint64_t bd = bdesc0 + (uint64_t)(r.s * kAtoms * bstep);
-          const uint32_t at = tmem + g.acol + 32 * kAtoms * r.s;
+        const uint64_t bd = bdesc0 + (uint64_t)(r.s * kAtoms * bstep);
+        const uint32_t at = tmem + g.acol + 32 * kAtoms * r.s;
+        if (elect_one()) {
           // per atom: four K=16 slices, 8 TMEM columns / 32 bytes apart
 #pragma unroll
           for (int a = 0; a < kAtoms; ++a) {
@@ -298,12 +320,21 @@ ibgemm_kernel(ICfg g, const __grid_constant__ CUtensorMap xmap, unsigned int* ti
           }
           mma_commit(&freeS[r.s]);
         }
-        mma_commit(&accfull[ab]);
+        __syncwarp();
+        // poll the next ring position now (its latency overlaps the loop)
+        Ring nx = r;
+        nx.next();
+        const bool pb = tma::mbar_try_wait(&fullB[nx.s], nx.ph);
+        const bool pa = tma::mbar_try_wait(&afull[nx.s], nx.ph);
+        polled = pb && pa;
       }
-      // every MMA must be done before the tensor memory is freed
-      mma_commit(&done);
-      wait_bar(&done, 0, nullptr, nullptr);
+      if (elect_one()) mma_commit(&accfull[ab]);
+      __syncwarp();
     }
+    // every MMA must be done before the tensor memory is freed
+    if (elect_one()) mma_commit(&done);
+    __syncwarp();
+    wait_bar(&done, 0, nullptr, nullptr);
     __syncwarp();
   } else if (warp >= kEpiWarp0) {
     // ---- epilogue: warp 8+q reads lanes 32q..32q+31 ------------------------
@@ -313,9 +344,9 @@ ibgemm_kernel(ICfg g, const __grid_constant__ CUtensorMap xmap, unsigned int* ti
     const int64_t plane = (int64_t)g.Ho * g.Wo;
     const int64_t nstride = g.out_ctot * plane;
     uint32_t tiles = 0;
-    for (int64_t u = u0; u < u1; ++u, ++tiles) {
-      const int64_t c = u / g.T;
-      const int t = (int)(u - c * g.T);
+    for (Units w(u0, u1, g.T); w.more(); w.next(), ++tiles) {
+      const int64_t c = w.c;
+      const int t = w.t;
       const int ab = tiles & (g.nacc - 1);
       const uint32_t ause = g.nacc == 2 ? tiles >> 1 : tiles;
       bool ok = !*abortp && wait_bar(&accfull[ab], ause & 1, timeouts, abortp, kSleepNs);
@@ -353,24 +384,27 @@ ibgemm_kernel(ICfg g, const __grid_constant__ CUtensorMap xmap, unsigned int* ti
     const uint32_t tlane = tmem + ((uint32_t)(quarter * 32) << 16) + g.acol + 32 * half;
     Ring r;
     int64_t cur_c = -1;
-    for (int64_t u = u0; u < u1; ++u) {
-      const int64_t c = u / g.T;
-      const int t = (int)(u - c * g.T);
+    for (Units w(u0, u1, g.T); w.more(); w.next()) {
+      const int64_t c = w.c;
+      const int t = w.t;
       if (c != cur_c) {
         // eight copies of the padded filter rows, copy s shifted left by s:
         // SC[s][dy][i] = fr(dy, i + s), fr(dy, j) = w'[dy][j - (Wo - 1 - pw)].
-        // Every builder has finished the previous channel's steps here.
+        // One warp per (s, dy) row. Every builder has finished the previous
+        // channel's steps here.
         builders_sync();
-        const T* wc = w + c * g.kh * g.kw;
-        const int per = g.kh * g.L;
-        for (int e = tid; e < 8 * per; e += kBuilders) {
-          const int s = e / per, rem = e - s * per;
-          const int dy = rem / g.L, i = rem - dy * g.L;
-          const int b = i + s - (g.Wo - 1 - g.pw);
-          float v = 0.f;
-          if (b >= 0 && b < g.kw)
-            v = g.flip ? ld(wc + (g.kh - 1 - dy) * g.kw + (g.kw - 1 - b)) : ld(wc + dy * g.kw + b);
-          SC[e] = from_f<T>(v);
+        const T* wc = w_ + c * g.kh * g.kw;
+        for (int row = warp; row < 8 * g.kh; row += kBuilders / 32) {
+          const int s = row / g.kh, dy = row - s * g.kh;
+          const T* wrow = g.flip ? wc + (g.kh - 1 - dy) * g.kw : wc + dy * g.kw;
+          T* dst = SC + (size_t)(s * g.kh + dy) * g.L;
+          const int b0 = s - (g.Wo - 1 - g.pw);  // filter column of element 0
+          for (int i = lane; i < g.L; i += 32) {
+            const int b = i + b0;
+            float v = 0.f;
+            if (b >= 0 && b < g.kw) v = ld(wrow + (g.flip ? g.kw - 1 - b : b));
+            dst[i] = from_f<T>(v);
+          }
         }
         builders_sync();
         cur_c = c;
