@@ -44,6 +44,7 @@ dwconv_status_t make_conv(const dwconv2d_desc_t* d, Conv* c) {
   v.m = d->multiplier; v.kh = d->kh; v.kw = d->kw;
   v.sh = d->stride_h; v.sw = d->stride_w; v.ph = d->pad_h; v.pw = d->pad_w;
   v.dh = d->dil_h; v.dw = d->dil_w; v.dtype = d->dtype;
+  v.dC = FastDiv((uint32_t)v.C);
   v.Ho = out_extent(v.H, v.kh, v.sh, v.ph, v.dh);
   v.Wo = out_extent(v.W, v.kw, v.sw, v.pw, v.dw);
   if (v.Ho < 1 || v.Wo < 1) return DWCONV_ERR_INVALID_ARG;

@@ -10,6 +10,32 @@
 
 namespace dwconv {
 
+// Division of 32-bit unsigned numerators by a divisor fixed at launch time,
+// as a multiply-high and two shifts (Granlund and Montgomery, "Division by
+// invariant integers using multiplication", PLDI 1994, section 4): with
+// l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1,
+// t = mulhi(m, n), q = (t + ((n - t) >> 1)) >> (l - 1), exact for all n < 2^32.
+struct FastDiv {
+  uint32_t d, m, s1, s2;
+  FastDiv() = default;
+  __host__ explicit FastDiv(uint32_t div) : d(div) {
+    uint32_t l = 0;
+    while ((uint64_t(1) << l) < div) ++l;
+    m = (uint32_t)(((uint64_t(1) << 32) * ((uint64_t(1) << l) - div)) / div + 1);
+    s1 = l > 0 ? 1u : 0u;
+    s2 = l > 0 ? l - 1 : 0u;
+  }
+  __device__ __forceinline__ uint32_t div(uint32_t n) const {
+    const uint32_t t = __umulhi(m, n);
+    return (t + ((n - t) >> s1)) >> s2;
+  }
+  // q = n / d, returns n - q * d
+  __device__ __forceinline__ uint32_t divmod(uint32_t n, uint32_t& q) const {
+    q = div(n);
+    return n - q * d;
+  }
+};
+
 // Validated convolution geometry, passed to kernels by value.
 struct Conv {
   int64_t N, C, H, W;
@@ -17,6 +43,17 @@ struct Conv {
   int64_t Ho, Wo;
   int64_t off, ctot;  // channel slice of y / gy
   int dtype;
+  FastDiv dC;         // division by C: plane index (n*C + c) -> (n, c)
+
+  // The tiled kernels index planes n*C + c in 32 bits.
+  __host__ __device__ bool planes32() const { return N * C * m < (int64_t(1) << 31); }
+  // plane index -> (sample, channel); valid when planes32()
+  __device__ __forceinline__ void split(int64_t pin, int64_t& n, int64_t& ch) const {
+    uint32_t q;
+    const uint32_t r = dC.divmod((uint32_t)pin, q);
+    n = q;
+    ch = r;
+  }
 
   __host__ __device__ int64_t OC() const { return C * m; }
   __host__ __device__ int64_t x_plane() const { return H * W; }
@@ -53,31 +90,7 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
 // plain (coherent) load for data this kernel may also write
 template <typename T> __device__ __forceinline__ float ld_rw(const T* p) { return to_f<T>(*p); }
 
-// Division of 32-bit unsigned numerators by a divisor fixed at launch time,
-// as a multiply-high and two shifts (Granlund and Montgomery, "Division by
-// invariant integers using multiplication", PLDI 1994, section 4): with
-// l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1,
-// t = mulhi(m, n), q = (t + ((n - t) >> 1)) >> (l - 1), exact for all n < 2^32.
-struct FastDiv {
-  uint32_t d, m, s1, s2;
-  FastDiv() = default;
-  __host__ explicit FastDiv(uint32_t div) : d(div) {
-    uint32_t l = 0;
-    while ((uint64_t(1) << l) < div) ++l;
-    m = (uint32_t)(((uint64_t(1) << 32) * ((uint64_t(1) << l) - div)) / div + 1);
-    s1 = l > 0 ? 1u : 0u;
-    s2 = l > 0 ? l - 1 : 0u;
-  }
-  __device__ __forceinline__ uint32_t div(uint32_t n) const {
-    const uint32_t t = __umulhi(m, n);
-    return (t + ((n - t) >> s1)) >> s2;
-  }
-  // q = n / d, returns n - q * d
-  __device__ __forceinline__ uint32_t divmod(uint32_t n, uint32_t& q) const {
-    q = div(n);
-    return n - q * d;
-  }
-};
+
 
 inline int div_up(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 

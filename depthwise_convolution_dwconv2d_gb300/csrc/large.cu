@@ -13,6 +13,7 @@ template <typename T>
 cudaError_t wgrad_t(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s);
 
 bool supported(const Conv& c) {
+  if (!c.planes32()) return false;
   // square kernels of the compiled sizes, stride 1, dilation 1, one filter per channel,
   // planes up to 128 x 128
   if (c.kh != c.kw) return false;

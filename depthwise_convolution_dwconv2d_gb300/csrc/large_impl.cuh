@@ -83,11 +83,13 @@ large_kernel(Conv c, LCfg g, const T* __restrict__ in, const T* __restrict__ w, 
   const int64_t nplanes = c.N * c.C;
   const int64_t units = g.groups;
   auto src_of = [&](int64_t pin) {
-    const int64_t n = pin / c.C, ch = pin - n * c.C;
+    int64_t n, ch;
+    c.split(pin, n, ch);
     return FLIP ? in + c.y_base(n, ch) : in + c.x_base(n, ch);
   };
   auto dst_of = [&](int64_t pin) {
-    const int64_t n = pin / c.C, ch = pin - n * c.C;
+    int64_t n, ch;
+    c.split(pin, n, ch);
     return FLIP ? out + c.x_base(n, ch) : out + c.y_base(n, ch);
   };
   auto issue = [&](int64_t u, float* dst) {
@@ -118,7 +120,9 @@ large_kernel(Conv c, LCfg g, const T* __restrict__ in, const T* __restrict__ w, 
       const float* t = cur + pl * g.tile_elems;
       const float* wt = t + g.wofs;
       const int oh0 = rbi * R, ow0 = cbi * V;
-      const float bv = bias ? ld(bias + (p0 + pl) % c.C) : 0.f;
+      int64_t n_, ch_;
+      c.split(p0 + pl, n_, ch_);
+      const float bv = bias ? ld(bias + ch_) : 0.f;
       float acc[R][V];
 #pragma unroll
       for (int r = 0; r < R; ++r)
@@ -265,13 +269,22 @@ large_wgrad_kernel(Conv c, WLCfg g, const T* __restrict__ x, const T* __restrict
   // the CTA's steps: (unit u, sample s in its chunk)
   int64_t u = blockIdx.x;
   int sidx = 0;
-  auto unit_n0 = [&](int64_t uu) { return (uu / c.C) * g.nb; };
+  // unit uu = chunk * C + channel
+  auto unit_n0 = [&](int64_t uu) {
+    uint32_t q;
+    c.dC.divmod((uint32_t)uu, q);
+    return (int64_t)q * g.nb;
+  };
+  auto unit_ch = [&](int64_t uu) {
+    uint32_t q;
+    return (int64_t)c.dC.divmod((uint32_t)uu, q);
+  };
   auto unit_ns = [&](int64_t uu) {
     const int64_t n0 = unit_n0(uu);
     const int64_t ns = (c.N - n0) < g.nb ? (c.N - n0) : g.nb;
     return (int)(ns > 0 ? ns : 0);
   };
-  if (u < units && unit_ns(u) > 0) issue(unit_n0(u) + sidx, u % c.C, buf0);
+  if (u < units && unit_ns(u) > 0) issue(unit_n0(u) + sidx, unit_ch(u), buf0);
   tile::cp_async_commit();
   const int tid = threadIdx.x;
   const int item = tid % g.items, grp = tid / g.items;
@@ -291,7 +304,7 @@ large_wgrad_kernel(Conv c, WLCfg g, const T* __restrict__ x, const T* __restrict
       sn = 0;
       un = u + gridDim.x;
     }
-    if (un < units && unit_ns(un) > 0) issue(unit_n0(un) + sn, un % c.C, (k & 1) ? buf0 : buf1);
+    if (un < units && unit_ns(un) > 0) issue(unit_n0(un) + sn, unit_ch(un), (k & 1) ? buf0 : buf1);
     tile::cp_async_commit();
     tile::cp_async_wait<1>();
     __syncthreads();
@@ -352,8 +365,9 @@ large_wgrad_kernel(Conv c, WLCfg g, const T* __restrict__ x, const T* __restrict
       float* wred = red + g.G * (K * K + 1);
       if ((tid & 31) == 0) wred[tid >> 5] = bv;
       __syncthreads();
-      const int chunk = (int)(u / c.C);
-      const int64_t ch = u % c.C;
+      uint32_t cq;
+      const int64_t ch = c.dC.divmod((uint32_t)u, cq);
+      const int chunk = (int)cq;
       float* dstp = ws + ((int64_t)chunk * c.OC() + ch) * (K * K + 1);
       for (int t = tid; t < K * K; t += kNT) {
         float sum = 0.f;

@@ -371,6 +371,30 @@ __device__ __forceinline__ void store_block(T* __restrict__ plane, int64_t Wo, i
   }
 }
 
+// Output staging for units of whole output planes that are contiguous in
+// memory but whose rows take no vector stores: the threads write their
+// results into a dense copy of the unit's planes in shared memory ...
+// ... and the CTA then writes the ne staged elements to dst with 4-element
+// vector stores (scalar head and tail up to the alignment), adding the old
+// values when add is set. Call after a barrier.
+template <typename T>
+__device__ __forceinline__ void flush_staged(T* __restrict__ dst, const T* __restrict__ src, int ne, bool add) {
+  constexpr int VB = 4 * sizeof(T);  // bytes per vector store
+  int head = (int)(((VB - (reinterpret_cast<uintptr_t>(dst) % VB)) % VB) / sizeof(T));
+  if (head > ne) head = ne;
+  const int nvec = (ne - head) / 4;
+  for (int i = threadIdx.x; i < head; i += kNT) dst[i] = add ? from_f<T>(to_f<T>(src[i]) + ld_rw(dst + i)) : src[i];
+  for (int i = threadIdx.x; i < nvec; i += kNT) {
+    const int e = head + 4 * i;
+    float f[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) f[q] = to_f<T>(src[e + q]) + (add ? ld_rw(dst + e + q) : 0.f);
+    store_vec<T, 4>(dst + e, f);
+  }
+  for (int i = head + 4 * nvec + threadIdx.x; i < ne; i += kNT)
+    dst[i] = add ? from_f<T>(to_f<T>(src[i]) + ld_rw(dst + i)) : src[i];
+}
+
 // ---- host-side planning -------------------------------------------------------
 inline int round_up(int64_t v, int m) { return (int)((v + m - 1) / m * m); }
 

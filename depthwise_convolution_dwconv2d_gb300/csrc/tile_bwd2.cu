@@ -22,6 +22,7 @@ template <typename T>
 cudaError_t bwd2_t(const Conv& c, const void* gy, const void* w, void* gx, bool acc, cudaStream_t s);
 
 bool bwd2_supported(const Conv& c) {
+  if (!c.planes32()) return false;
   if (c.kh != c.kw || c.sh != c.sw || c.dh != c.dw || c.sh < 2 || c.m > 4) return false;
   if (c.W > 1024 || c.Wo > 1024) return false;
   if (c.ph % c.sh != c.pw % c.sh) return false;

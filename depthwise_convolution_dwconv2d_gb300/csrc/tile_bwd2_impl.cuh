@@ -49,6 +49,9 @@ struct Bwd2Cfg {
   FastDiv trdiv, d_plane, d_cb, d_bands;
   uint32_t tma_bytes;
   int seg, stg_elems;  // dense staging of whole grad_out planes
+  int tab_floats;      // per-stage filter table: ppc*m*K*K floats (rounded)
+  int ostage;          // results of whole gx planes go through shared memory
+  int ostg_elems;      // size of that output staging buffer (elements)
 };
 
 template <typename T, int K, int S, int D, int PM, int R, int V, int DL>
@@ -72,26 +75,42 @@ bwd2_kernel(Conv c, Bwd2Cfg g, const __grid_constant__ CUtensorMap tmap, unsigne
   T* const buf1 = buf0 + g.stage_elems;
   T* const stg0 = buf1 + g.stage_elems;
   T* const stg1 = stg0 + g.stg_elems;
+  // per stage: the filters of the stage's (plane, j) pairs; then the output
+  // staging buffer (whole gx planes of one unit, written out coalesced)
+  float* const tab0 = reinterpret_cast<float*>(stg1 + g.stg_elems);
+  float* const tab1 = tab0 + g.tab_floats;
+  T* const ostg = reinterpret_cast<T*>(tab1 + g.tab_floats);
   const int64_t nplanes = c.N * c.C;
   const int64_t units = g.groups * g.nbands;
   const int m = c.m;
   auto gy_plane = [&](int64_t p0, int s) {
-    const int pl = s / m, j = s - pl * m;
-    const int64_t pin = p0 + pl, n = pin / c.C, ch = pin - n * c.C;
+    const int pl = m == 1 ? s : s / m, j = s - pl * m;
+    int64_t n, ch;
+    c.split(p0 + pl, n, ch);
     return gy + c.y_base(n, ch * m + j);
   };
-  auto issue = [&](int64_t u, T* dst, T* stg, uint64_t* bar) {
+  auto issue = [&](int64_t u, T* dst, T* stg, float* tab, uint64_t* bar) {
     uint32_t grp;
     const int band = (int)g.d_bands.divmod((uint32_t)u, grp);
     const int64_t p0 = (int64_t)grp * g.ppc;
     const int np = (int)((nplanes - p0) < g.ppc ? (nplanes - p0) : g.ppc);
+    // one (plane, j) filter per thread
+    for (int sj = threadIdx.x; sj < np * m; sj += kNT) {
+      const int pl = m == 1 ? sj : sj / m;
+      int64_t n, ch;
+      c.split(p0 + pl, n, ch);
+      const T* wp = w + (ch * m + (sj - pl * m)) * (K * K);
+#pragma unroll
+      for (int i = 0; i < K * K; ++i) tab[sj * (K * K) + i] = ld(wp + i);
+    }
     if (g.mode == kCopyDense) {
       issue_flat<T>(stg, np * m, g.seg, [&](int s) { return gy_plane(p0, s); }, (int)(c.Ho * c.Wo));
       return;
     }
     if (use_tma) {
       if (threadIdx.x == 0) {
-        const int64_t n = p0 / c.C, ch = p0 - n * c.C;  // units never straddle samples
+        int64_t n, ch;
+        c.split(p0, n, ch);  // units never straddle samples
         tma::fence_async_smem();
         tma::mbar_expect_tx(bar, g.tma_bytes);
         tma::load_3d(dst, &tmap, g.ix0, band * g.thu + g.row0, (int)(n * c.ctot + c.off + ch * m), bar);
@@ -99,20 +118,19 @@ bwd2_kernel(Conv c, Bwd2Cfg g, const __grid_constant__ CUtensorMap tmap, unsigne
       return;
     }
     issue_tile<T>(dst, np * m, g.tile_elems, g.pitch,
-                  [&](int s) {
-                    const int pl = s / m, j = s - pl * m;
-                    const int64_t pin = p0 + pl, n = pin / c.C, ch = pin - n * c.C;
-                    return gy + c.y_base(n, ch * m + j);
-                  },
+                  [&](int s) { return gy_plane(p0, s); },
                   (int)c.Ho, (int)c.Wo, band * g.thu + g.row0, g.tr, g.trdiv, g.ix0, g.mode);
   };
   int64_t u = blockIdx.x;
-  if (u < units) issue(u, buf0, stg0, &bars[0]);
+  if (u < units) issue(u, buf0, stg0, tab0, &bars[0]);
   cp_async_commit();
   for (int k = 0; u < units; ++k, u += gridDim.x) {
     T* cur = (k & 1) ? buf1 : buf0;
+    const float* tab = (k & 1) ? tab1 : tab0;
     const bool more = u + gridDim.x < units;
-    if (more) issue(u + gridDim.x, (k & 1) ? buf0 : buf1, (k & 1) ? stg0 : stg1, &bars[(k + 1) & 1]);
+    if (more)
+      issue(u + gridDim.x, (k & 1) ? buf0 : buf1, (k & 1) ? stg0 : stg1, (k & 1) ? tab0 : tab1,
+            &bars[(k + 1) & 1]);
     cp_async_commit();
     cp_async_wait<1>();
     if (use_tma && !tma::mbar_wait(&bars[k & 1], (uint32_t)(k >> 1) & 1, timeouts)) {
@@ -129,7 +147,6 @@ bwd2_kernel(Conv c, Bwd2Cfg g, const __grid_constant__ CUtensorMap tmap, unsigne
     const bool dense = g.mode == kCopyDense;
     const int total = np * (int)g.d_plane.d;
     float wr[K * K];
-    int cur_pl = -1;
     for (int it = threadIdx.x; it < total; it += kNT) {
       uint32_t pl_, rbi_;
       const uint32_t rem = g.d_plane.divmod((uint32_t)it, pl_);
@@ -146,12 +163,8 @@ bwd2_kernel(Conv c, Bwd2Cfg g, const __grid_constant__ CUtensorMap tmap, unsigne
 #pragma unroll
             for (int pw = 0; pw < S; ++pw) acc[r][ph][v][pw] = 0.f;
       for (int j = 0; j < m; ++j) {
-        if (m > 1 || pl != cur_pl) {
-          const int64_t oc = (pin % c.C) * m + j;
 #pragma unroll
-          for (int i = 0; i < K * K; ++i) wr[i] = ld(w + oc * (K * K) + i);
-          cur_pl = pl;
-        }
+        for (int i = 0; i < K * K; ++i) wr[i] = tab[(pl * m + j) * (K * K) + i];
         const T* t = cur + (pl * m + j) * g.tile_elems + (rbi * R) * g.pitch + cbi * V + g.cshift;
         // dense: grad_out plane coordinates of window (0, 0)
         const T* dp = dense ? dense_plane(stg, g.seg, pl * m + j, gy_plane(p0, pl * m + j)) : nullptr;
@@ -191,8 +204,26 @@ bwd2_kernel(Conv c, Bwd2Cfg g, const __grid_constant__ CUtensorMap tmap, unsigne
         }
       }
       // store rows S*(u0 + rbi*R + r) + ph, cols S*cbi*V .. + S*V
-      T* plane = gx + pin * c.H * c.W;
       const int col0 = S * V * cbi;
+      if (g.ostage) {
+        T* plane = ostg + pl * (int)(c.H * c.W);
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int ph = 0; ph < S; ++ph) {
+            const int ih = S * (u0 + rbi * R + r) + ph;
+            if (ih >= c.H) continue;
+#pragma unroll
+            for (int v = 0; v < V; ++v)
+#pragma unroll
+              for (int pw = 0; pw < S; ++pw) {
+                const int iw = col0 + v * S + pw;
+                if (iw < c.W) plane[ih * c.W + iw] = from_f<T>(acc[r][ph][v][pw]);
+              }
+          }
+        continue;
+      }
+      T* plane = gx + pin * c.H * c.W;
 #pragma unroll
       for (int r = 0; r < R; ++r)
 #pragma unroll
@@ -223,6 +254,11 @@ bwd2_kernel(Conv c, Bwd2Cfg g, const __grid_constant__ CUtensorMap tmap, unsigne
           }
         }
     }
+    if (g.ostage) {
+      // the unit's gx planes are contiguous in memory
+      __syncthreads();
+      flush_staged<T>(gx + p0 * c.H * c.W, ostg, np * (int)(c.H * c.W), accumulate);
+    }
     __syncthreads();
   }
 }
@@ -231,7 +267,8 @@ template <typename T, int K, int S, int D, int PM, int DL>
 cudaError_t launch_bwd2(const Conv& c, const Bwd2Cfg& g, const CUtensorMap& map, const void* gy,
                         const void* w, void* gx, bool acc, cudaStream_t s) {
   auto kern = bwd2_kernel<T, K, S, D, PM, 2, 4, DL>;
-  const size_t smem = 128 + 2 * ((size_t)g.stage_elems + g.stg_elems) * sizeof(T);
+  const size_t smem = 128 + 2 * ((size_t)g.stage_elems + g.stg_elems) * sizeof(T) + 2 * (size_t)g.tab_floats * 4 +
+                      (size_t)g.ostg_elems * sizeof(T);
   cudaError_t e = set_smem(kern, smem);
   if (e != cudaSuccess) return e;
   const int grid = persistent_grid(kern, smem, g.groups * g.nbands);
@@ -308,6 +345,11 @@ cudaError_t run_bwd2_t(const Conv& c, const void* gy, const void* w, void* gx, b
   g.tma_bytes = (uint32_t)((int64_t)g.ppc * c.m * g.tile_elems * ES);
   g.stg_elems = g.mode == kCopyDense ? stage_round((int64_t)g.ppc * c.m * g.seg, ES) : 0;
   g.vec_out = (reinterpret_cast<uintptr_t>(gx) % (4 * ES) == 0) && c.W % 4 == 0;
+  g.tab_floats = round_up((int64_t)g.ppc * c.m * K * K, 4);
+  // small gx planes whose rows take no vector stores: whole planes through
+  // shared memory (units are whole planes when there is one band)
+  g.ostage = !g.vec_out && g.nbands == 1 && (int64_t)g.ppc * c.H * c.W * ES <= 64 * 1024;
+  g.ostg_elems = g.ostage ? stage_round((int64_t)g.ppc * c.H * c.W, ES) : 0;
   switch (dl) {
     case 0: return launch_bwd2<T, K, S, D, PM, 0>(c, g, map, gy, w, gx, acc, s);
     case 1: return launch_bwd2<T, K, S, D, PM, 1>(c, g, map, gy, w, gx, acc, s);

@@ -19,6 +19,7 @@ bool square(const Conv& c) {
 }  // namespace
 
 bool fwd_supported(const Conv& c) {
+  if (!c.planes32()) return false;
   if (!square(c) || c.W > 1024 || c.Wo > 1024) return false;
 #define X(K, S, D) if (c.kh == K && c.sh == S && c.dh == D) return true;
   DW_FWD_CASES(X)
@@ -33,6 +34,7 @@ cudaError_t fwd(const Conv& c, const void* x, const void* w, const void* b, void
 }
 
 bool bwd1_supported(const Conv& c) {
+  if (!c.planes32()) return false;
   if (!square(c) || c.sh != 1 || c.m > 4 || c.W > 1024 || c.Wo > 1024) return false;
   if (c.ph > c.dh * (c.kh - 1) || c.pw > c.dw * (c.kw - 1)) return false;
 #define X(K, D) if (c.kh == K && c.dh == D) return true;

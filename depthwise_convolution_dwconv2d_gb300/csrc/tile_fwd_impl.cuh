@@ -71,16 +71,15 @@ fwd_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned int
     float* wt = tab;
     float* bt = tab + nout * (K * K);
     int64_t* ot = reinterpret_cast<int64_t*>(tab + g.tab_off64);
-    for (int i = threadIdx.x; i < np * c.m * (K * K); i += kNT) {
-      const int pj = i / (K * K), tap = i - pj * (K * K);
-      const int64_t pin = p0 + pj / c.m;
-      const int64_t oc = (pin % c.C) * c.m + pj % c.m;
-      wt[i] = ld(w + oc * (K * K) + tap);
-    }
+    // one output plane per thread: its taps, bias and output offset
     for (int pj = threadIdx.x; pj < np * c.m; pj += kNT) {
-      const int64_t pin = p0 + pj / c.m;
-      const int64_t n = pin / c.C;
-      const int64_t oc = (pin - n * c.C) * c.m + pj % c.m;
+      const int pl = c.m == 1 ? pj : pj / c.m;
+      int64_t n, ch;
+      c.split(p0 + pl, n, ch);
+      const int64_t oc = ch * c.m + (pj - pl * c.m);
+      const T* wp = w + oc * (K * K);
+#pragma unroll
+      for (int tap = 0; tap < K * K; ++tap) wt[pj * (K * K) + tap] = ld(wp + tap);
       bt[pj] = bias ? ld(bias + oc) : 0.f;
       ot[pj] = c.y_base(n, oc);
     }
@@ -173,8 +172,9 @@ bwd1_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned in
   const int64_t units = g.groups * g.nbands;
   const int m = c.m;
   auto gy_plane = [&](int64_t p0, int s) {
-    const int pl = s / m, j = s - pl * m;
-    const int64_t pin = p0 + pl, n = pin / c.C, ch = pin - n * c.C;
+    const int pl = m == 1 ? s : s / m, j = s - pl * m;
+    int64_t n, ch;
+    c.split(p0 + pl, n, ch);
     return gy + c.y_base(n, ch * m + j);
   };
   auto issue = [&](int64_t u, T* dst, T* stg, float* tab, uint64_t* bar) {
@@ -187,26 +187,26 @@ bwd1_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned in
       issue_flat<T>(stg, np * m, g.seg, [&](int s) { return gy_plane(p0, s); }, (int)(c.Ho * c.Wo));
     } else if (use_tma) {
       if (threadIdx.x == 0) {
-        const int64_t n = p0 / c.C, ch = p0 - n * c.C;  // units never straddle samples
+        int64_t n, ch;
+        c.split(p0, n, ch);  // units never straddle samples
         tma::fence_async_smem();
         tma::mbar_expect_tx(bar, g.tma_bytes);
         tma::load_3d(dst, &tmap, g.ix0, band * g.th - qh, (int)(n * c.ctot + c.off + ch * m), bar);
       }
     } else {
       issue_tile<T>(dst, np * m, g.tile_elems, g.pitch,
-                    [&](int s) {
-                      const int pl = s / m, j = s - pl * m;
-                      const int64_t pin = p0 + pl, n = pin / c.C, ch = pin - n * c.C;
-                      return gy + c.y_base(n, ch * m + j);
-                    },
+                    [&](int s) { return gy_plane(p0, s); },
                     (int)c.Ho, (int)c.Wo, band * g.th - qh, g.tr, g.trdiv, g.ix0, g.mode);
     }
     int64_t* ot = reinterpret_cast<int64_t*>(tab + g.tab_off64);
-    for (int i = threadIdx.x; i < np * m * (K * K); i += kNT) {
-      const int s = i / (K * K), tap = i - s * (K * K);
-      const int64_t pin = p0 + s / m;
-      const int64_t oc = (pin % c.C) * m + s % m;
-      tab[i] = ld(w + oc * (K * K) + (K * K - 1 - tap));
+    // one staged plane per thread: its rotated filter
+    for (int s = threadIdx.x; s < np * m; s += kNT) {
+      const int pl = m == 1 ? s : s / m;
+      int64_t n, ch;
+      c.split(p0 + pl, n, ch);
+      const T* wp = w + (ch * m + (s - pl * m)) * (K * K);
+#pragma unroll
+      for (int tap = 0; tap < K * K; ++tap) tab[s * (K * K) + tap] = ld(wp + (K * K - 1 - tap));
     }
     for (int pl = threadIdx.x; pl < np; pl += kNT) ot[pl] = (p0 + pl) * c.H * c.W;
   };
@@ -296,6 +296,7 @@ cudaError_t run_fwd_t(const Conv& c, const void* x, const void* w, const void* b
   if (!plan_tile<T, K, S, D, R, V>(c.N * c.C, 1, c.m, c.H, c.W, c.Ho, c.Wo, c.pw, x, vout, &g, &dl, 0,
                                    c.N * c.C, &map))
     return cudaErrorInvalidConfiguration;
+
   switch (dl) {
     case 0: return launch_fwd<T, K, S, D, 0>(c, g, map, x, w, b, y, s);
     case 1: return launch_fwd<T, K, S, D, Q == 1 ? 1 : 0>(c, g, map, x, w, b, y, s);
@@ -331,6 +332,7 @@ cudaError_t run_bwd1_t(const Conv& c, const void* gy, const void* w, void* gx, b
   if (!plan_tile<T, K, 1, D, R, V>(c.N * c.C, c.m, 1, c.Ho, c.Wo, c.H, c.W, qw, gy, vout, &g, &dl, c.C,
                                    c.N * c.ctot, &map))
     return cudaErrorInvalidConfiguration;
+
   switch (dl) {
     case 0: return launch_bwd1<T, K, D, 0>(c, g, map, qh, gy, w, gx, acc, s);
     case 1: return launch_bwd1<T, K, D, Q == 1 ? 1 : 0>(c, g, map, qh, gy, w, gx, acc, s);

@@ -122,7 +122,8 @@ fwd_multi_kernel(Conv c, MCfg g, MultiArgs a, const T* __restrict__ x, T* __rest
     for (int it = threadIdx.x; it < np * per_plane; it += kNT) {
       const int pl = it / per_plane;
       const int q = it - pl * per_plane;
-      const int64_t pin = p0 + pl, n = pin / c.C, ch = pin - n * c.C;
+      int64_t n, ch;
+      c.split(p0 + pl, n, ch);
       const T* t = cur + pl * g.tile_elems;
       if (q < i0) {
         fwd_branch<K, D0>(c, a, 0, t, g.pitch, q, n, ch, oh0, band_rows, (const T*)a.w[0],
@@ -157,7 +158,8 @@ bwd_multi_kernel(Conv c, MCfg g, MultiArgs a, const T* __restrict__ gy, T* gx) {
       const int boff = b == 0 ? 0 : (b == 1 ? a.tile_elems[0] : a.tile_elems[0] + a.tile_elems[1]);
       issue_tile<T>(dst + boff, np, slice, g.pitch,
                     [&](int p) {
-                      const int64_t pin = p0 + p, n = pin / c.C, ch = pin - n * c.C;
+                      int64_t n, ch;
+                      c.split(p0 + p, n, ch);
                       return gy + (n * c.ctot + a.off[b] + ch) * c.Ho * c.Wo;
                     },
                     (int)c.Ho, (int)c.Wo, band * g.th + a.iy0[b], a.tr[b], a.trdiv[b], a.ix0[b],
@@ -186,7 +188,9 @@ bwd_multi_kernel(Conv c, MCfg g, MultiArgs a, const T* __restrict__ gy, T* gx) {
       const uint32_t rem = g.d_item.divmod((uint32_t)it, pl_);
       const int cbi = (int)g.d_cb.divmod(rem, rbi_);
       const int pl = (int)pl_, rbi = (int)rbi_;
-      const int64_t pin = p0 + pl, ch = pin % c.C;
+      const int64_t pin = p0 + pl;
+      int64_t n_, ch;
+      c.split(pin, n_, ch);
       if (pl != curp) {
         curp = pl;
 #pragma unroll
@@ -416,7 +420,7 @@ cudaError_t bwd_multi_t(int nb, const Conv* cs, const void* gy, const void* cons
 }  // namespace
 
 bool multi_supported(int nb, const Conv* cs) {
-  if (!same_geometry(nb, cs)) return false;
+  if (!same_geometry(nb, cs) || !cs[0].planes32()) return false;
   for (int b = 0; b < nb; ++b) {
     if (cs[b].kh != cs[0].kh) return false;
     // the fused grad-input needs non-negative transposed padding

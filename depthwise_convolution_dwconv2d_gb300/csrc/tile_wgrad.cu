@@ -27,6 +27,7 @@ template <typename T, int MSEL>
 cudaError_t wgrad_sel_t(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s);
 
 bool wgrad_supported(const Conv& c) {
+  if (!c.planes32()) return false;
   if (c.kh != c.kw || c.sh != c.sw || c.dh != c.dw || c.W > 1024 || c.Wo > 1024) return false;
 #define X(K, S, D, M) if (c.kh == K && c.sh == S && c.dh == D && c.m == M) return true;
   DW_WGRAD_CASES(X)
@@ -35,9 +36,10 @@ bool wgrad_supported(const Conv& c) {
 }
 
 int wgrad_chunks(const Conv& c) {
-  // about four units per SM over channels x chunks, each thread's serial
-  // chain (samples x positions / threads) far below 4096 terms
-  int64_t chunks = (152 * 4 + c.C - 1) / c.C;
+  // about sixteen units per SM over channels x chunks (so the last wave of
+  // units is a small part of the launch), each thread's serial chain
+  // (samples x positions / threads) far below 4096 terms
+  int64_t chunks = (152 * 16 + c.C - 1) / c.C;
   if (chunks > c.N) chunks = c.N;
   if (chunks < 1) chunks = 1;
   int64_t nb = (c.N + chunks - 1) / chunks;

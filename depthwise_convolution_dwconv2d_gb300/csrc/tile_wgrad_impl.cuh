@@ -43,7 +43,7 @@ struct WCfg {
   uint32_t tma_slice_bytes; // bytes per slice (banded planes)
   int xseg, gseg;           // dense staging segment sizes (x, grad_out)
   int stg_off, gstg_off;    // element offsets of the dense staging regions in a stage
-  FastDiv trdiv, thdiv, d_per, d_cb;
+  FastDiv trdiv, thdiv, d_per, d_cb, d_nbands;
 };
 
 template <typename T, int K, int S, int D, int M, int R, int V, int DL>
@@ -69,15 +69,25 @@ wgrad_kernel(Conv c, WCfg g, const __grid_constant__ CUtensorMap xmap,
   float* red = reinterpret_cast<float*>(reinterpret_cast<T*>(smraw) + 2 * g.stage_elems);  // [warps][NV]
   const int64_t units = c.C * g.chunks;
   // slices of a unit: (sample n0 + sl / nbands, band sl % nbands)
+  // unit u = chunk * C + channel (units < 2^32: the host caps chunks)
+  auto unit_split = [&](int64_t uu, int64_t& ch, int& chunk) {
+    uint32_t q;
+    ch = c.dC.divmod((uint32_t)uu, q);
+    chunk = (int)q;
+  };
   auto unit_slices = [&](int64_t u) {
-    const int chunk = (int)(u / c.C);
+    int64_t ch_;
+    int chunk;
+    unit_split(u, ch_, chunk);
     const int64_t n0 = (int64_t)chunk * g.nb;
     const int64_t nn = (c.N - n0) < g.nb ? (c.N - n0) : g.nb;
     return nn > 0 ? (int)(nn * g.nbands) : 0;
   };
   auto issue = [&](int64_t u, int s0, T* dst, uint64_t* bar) {
-    const int64_t ch = u % c.C;
-    const int64_t n0 = (u / c.C) * g.nb;
+    int64_t ch;
+    int chunk;
+    unit_split(u, ch, chunk);
+    const int64_t n0 = (int64_t)chunk * g.nb;
     const int nsl = unit_slices(u);
     const int ns = (nsl - s0) < g.ppc ? (nsl - s0) : g.ppc;
     T* xs = dst;
@@ -111,8 +121,9 @@ wgrad_kernel(Conv c, WCfg g, const __grid_constant__ CUtensorMap xmap,
           tma::mbar_expect_tx(bar, g.tma_slice_bytes * ns);
           for (int q = 0; q < ns; ++q) {
             const int sl = s0 + q;
-            const int n = (int)(n0 + sl / g.nbands);
-            const int oh0 = (sl % g.nbands) * g.th;
+            uint32_t sq;
+            const int oh0 = (int)g.d_nbands.divmod((uint32_t)sl, sq) * g.th;
+            const int n = (int)(n0 + sq);
             tma::load_4d(xs + q * g.xstride, &xmap, g.xix0, oh0 * S - c.ph, (int)ch, n, bar);
             tma::load_4d(gs + q * g.gstride, &gmap, 0, oh0, (int)(c.off + ch * M), n, bar);
           }
@@ -127,8 +138,9 @@ wgrad_kernel(Conv c, WCfg g, const __grid_constant__ CUtensorMap xmap,
     } else {
       for (int q = 0; q < ns; ++q) {
         const int sl = s0 + q;
-        const int64_t n = n0 + sl / g.nbands;
-        const int oh0 = (sl % g.nbands) * g.th;
+        uint32_t sq;
+        const int oh0 = (int)g.d_nbands.divmod((uint32_t)sl, sq) * g.th;
+        const int64_t n = n0 + sq;
         issue_tile<T>(xs + q * g.xstride, 1, g.xstride, g.pitch, [&](int) { return x + c.x_base(n, ch); },
                       (int)c.H, (int)c.W, oh0 * S - c.ph, g.tr, g.trdiv, g.xix0, g.xmode);
         issue_tile<T>(gs + q * g.gstride, M, g.g_elems, g.gpitch,
@@ -172,8 +184,10 @@ wgrad_kernel(Conv c, WCfg g, const __grid_constant__ CUtensorMap xmap,
     const T* gs = xs + g.goff;
     const int nsl = unit_slices(u);
     const int ns = (nsl - s0) < g.ppc ? (nsl - s0) : g.ppc;
-    const int64_t chu = u % c.C;
-    const int64_t n0u = (u / c.C) * g.nb;
+    int64_t chu;
+    int chunku;
+    unit_split(u, chu, chunku);
+    const int64_t n0u = (int64_t)chunku * g.nb;
     const int per = (int)g.d_per.d;
     for (int it = threadIdx.x; it < ns * per; it += kNT) {
       uint32_t q_, rbi_;
@@ -259,8 +273,9 @@ wgrad_kernel(Conv c, WCfg g, const __grid_constant__ CUtensorMap xmap,
           acc[j][i] = 0.f;
         }
       __syncthreads();
-      const int64_t ch = u % c.C;
-      const int chunk = (int)(u / c.C);
+      int64_t ch;
+      int chunk;
+      unit_split(u, ch, chunk);
       for (int i = threadIdx.x; i < NV; i += kNT) {
         float sum = 0.f;
         for (int wi = 0; wi < kNT / 32; ++wi) sum += red[wi * NV + i];
@@ -320,6 +335,7 @@ cudaError_t run_wgrad_t(const Conv& c, const void* x, const void* gy, float* ws,
   g.th = (int)th;
   g.rb = (int)(th / R);
   g.nbands = (int)((c.Ho + th - 1) / th);
+  g.d_nbands = FastDiv((uint32_t)g.nbands);
   g.tr = (int)tr_of(th);
   g.x_elems = g.tr * g.pitch;
   g.g_elems = (int)(th * g.gpitch);
