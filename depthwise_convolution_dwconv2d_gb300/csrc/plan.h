@@ -47,6 +47,7 @@ cudaError_t bwd2(const Conv& c, const void* gy, const void* w, void* gx, bool ac
 // tile_wgrad.cu (first pass; the second pass is bwd_weight_pass2)
 bool wgrad_supported(const Conv& c);
 int wgrad_chunks(const Conv& c);
+int64_t wgrad_nb(const Conv& c);  // samples per chunk (chunks = ceil(N / wgrad_nb))
 cudaError_t wgrad(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s);
 // tile_multi.cu
 bool multi_supported(int nb, const Conv* cs);

@@ -35,7 +35,7 @@ bool wgrad_supported(const Conv& c) {
   return false;
 }
 
-int wgrad_chunks(const Conv& c) {
+int64_t wgrad_nb(const Conv& c) {
   // about sixteen units per SM over channels x chunks (so the last wave of
   // units is a small part of the launch), each thread's serial chain
   // (samples x positions / threads) far below 4096 terms
@@ -43,11 +43,24 @@ int wgrad_chunks(const Conv& c) {
   if (chunks > c.N) chunks = c.N;
   if (chunks < 1) chunks = 1;
   int64_t nb = (c.N + chunks - 1) / chunks;
+  // whole planes staged a few samples at a time: make a chunk a whole number
+  // of stages (each stage about two items per thread; a block is R x 4
+  // outputs, R = 2 at stride 1)
+  const int64_t R = c.sh == 1 ? 2 : 1;
+  const int64_t items = (c.Ho + R - 1) / R * ((c.Wo + 3) / 4);
+  const int64_t spp = (2 * 256 + items - 1) / items;  // samples per stage
+  if (spp > 1 && nb % spp != 0) nb = (nb + spp - 1) / spp * spp;
+  if (nb > c.N) nb = c.N;
   const int64_t cap = ((int64_t)1 << 20) / (c.Ho * c.Wo > 0 ? c.Ho * c.Wo : 1);
   if (nb > cap) nb = cap > 0 ? cap : 1;
-  chunks = c.N > 0 ? (c.N + nb - 1) / nb : 1;
-  if (chunks > 65535) chunks = 65535;
-  return (int)chunks;
+  if (nb < 1) nb = 1;
+  if (c.N > 0 && (c.N + nb - 1) / nb > 65535) nb = (c.N + 65534) / 65535;
+  return nb;
+}
+
+int wgrad_chunks(const Conv& c) {
+  const int64_t nb = wgrad_nb(c);
+  return c.N > 0 ? (int)((c.N + nb - 1) / nb) : 1;
 }
 
 cudaError_t wgrad(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s) {

@@ -312,7 +312,8 @@ cudaError_t run_wgrad_t(const Conv& c, const void* x, const void* gy, float* ws,
   constexpr int PA = 16 / ES > 4 ? 16 / ES : 4;  // pitch alignment (elements)
   WCfg g{};
   g.chunks = chunks;
-  g.nb = (int)((c.N + chunks - 1) / chunks);
+  g.nb = (int)wgrad_nb(c);
+  if (c.N > 0 && (c.N + g.nb - 1) / g.nb != chunks) return cudaErrorInvalidConfiguration;
   g.cb = (int)((c.Wo + V - 1) / V);
   g.gpitch = round_up((int64_t)g.cb * V, PA);
   int ix0 = 0, shift = 0, gshift = 0;
@@ -354,9 +355,8 @@ cudaError_t run_wgrad_t(const Conv& c, const void* x, const void* gy, float* ws,
   alignas(64) CUtensorMap xmap{}, gmap{};
   g.tma = g.xmode == kCopy16 && g.gmode == kCopy16 && g.pitch <= 256 && g.tr <= 256 && g.gpitch <= 256 &&
           g.th <= 256 && ppc <= 256;
-  if (g.tma && g.nbands == 1) {
-    while (ppc > 1 && g.nb % ppc != 0) --ppc;  // whole stages only: boxes never run past a chunk
-  }
+  // (a chunk's last box may run past the chunk: the extra samples are
+  // copied but not used, and samples past the batch are zero-filled)
   if (g.tma) {
     const uint32_t bp = g.nbands == 1 ? (uint32_t)ppc : 1u;
     g.tma = tma::encode_4d(&xmap, x, c.dtype, c.W, c.H, c.C, c.N, g.pitch, g.tr, 1, bp) &&
