@@ -130,6 +130,28 @@ __device__ __forceinline__ void issue_flat(T* __restrict__ stg, int np, int seg,
   }
 }
 
+// Dense staging of planes that are one contiguous run in memory (n_elems
+// elements from src0): every thread copies 16-byte chunks of the run, so
+// small planes do not leave most lanes of a warp idle. Plane data then sits
+// at dense_at(stg, src0, offset).
+template <typename T>
+__device__ __forceinline__ void issue_contig(T* __restrict__ stg, const T* src0, int64_t n_elems) {
+  const char* a = reinterpret_cast<const char*>(src0);
+  const char* a0 = reinterpret_cast<const char*>(reinterpret_cast<uintptr_t>(a) & ~uintptr_t(15));
+  const char* end = a + n_elems * (int64_t)sizeof(T);
+  const int nch = (int)((end - a0 + 15) / 16);
+  char* d = reinterpret_cast<char*>(stg);
+  for (int k = threadIdx.x; k < nch; k += blockDim.x) {
+    const int64_t left = end - (a0 + 16 * k);
+    cp_async16(d + 16 * k, a0 + 16 * k, left >= 16 ? 16 : (int)left);
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ const T* dense_at(const T* stg, const T* src0, int off) {
+  return stg + (int)((reinterpret_cast<uintptr_t>(src0) & 15) / sizeof(T)) + off;
+}
+
 template <typename T, typename SrcOf>
 __device__ __forceinline__ void repitch(T* __restrict__ dst, int np, int plane_elems, int pitch,
                                         const T* __restrict__ stg, int seg, SrcOf src_of, int H, int W,
@@ -370,6 +392,41 @@ __device__ __forceinline__ void store_block(T* __restrict__ plane, int64_t Wo, i
     }
   }
 }
+
+// Work of one persistent CTA, stage by stage. Either units
+// u = blockIdx.x + k*gridDim.x of (plane group, band) pairs, or -- when a
+// plane is one band and the copies are not tensor copies -- an equal
+// contiguous share of the planes, staged ppc planes at a time, so every CTA
+// does the same work to within one plane (no tail of idle CTAs).
+struct Sched {
+  int64_t nplanes, units;
+  int ppc;
+  int balanced;
+  FastDiv d_bands;
+  int64_t pb, pe;  // this CTA's share of the planes (balanced)
+  __device__ __forceinline__ Sched(int64_t nplanes_, int64_t units_, int ppc_, int balanced_, FastDiv d_bands_)
+      : nplanes(nplanes_), units(units_), ppc(ppc_), balanced(balanced_), d_bands(d_bands_) {
+    pb = (int64_t)blockIdx.x * nplanes / gridDim.x;
+    pe = (int64_t)(blockIdx.x + 1) * nplanes / gridDim.x;
+  }
+  // stage k of this CTA: first plane, plane count and band; false when done
+  __device__ __forceinline__ bool stage(int k, int64_t& p0, int& np, int& band) const {
+    if (balanced) {
+      p0 = pb + (int64_t)k * ppc;
+      if (p0 >= pe) return false;
+      np = (int)((pe - p0) < ppc ? (pe - p0) : ppc);
+      band = 0;
+      return true;
+    }
+    const int64_t u = blockIdx.x + (int64_t)k * gridDim.x;
+    if (u >= units) return false;
+    uint32_t grp;
+    band = (int)d_bands.divmod((uint32_t)u, grp);
+    p0 = (int64_t)grp * ppc;
+    np = (int)((nplanes - p0) < ppc ? (nplanes - p0) : ppc);
+    return true;
+  }
+};
 
 // Output staging for units of whole output planes that are contiguous in
 // memory but whose rows take no vector stores: the threads write their

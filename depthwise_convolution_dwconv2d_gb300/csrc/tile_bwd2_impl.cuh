@@ -49,6 +49,8 @@ struct Bwd2Cfg {
   FastDiv trdiv, d_plane, d_cb, d_bands;
   uint32_t tma_bytes;
   int seg, stg_elems;  // dense staging of whole grad_out planes
+  int balanced;        // equal contiguous plane shares per CTA (see Sched)
+  int contig;          // dense staging: a stage's planes are one contiguous run
   int tab_floats;      // per-stage filter table: ppc*m*K*K floats (rounded)
   int ostage;          // results of whole gx planes go through shared memory
   int ostg_elems;      // size of that output staging buffer (elements)
@@ -89,11 +91,7 @@ bwd2_kernel(Conv c, Bwd2Cfg g, const __grid_constant__ CUtensorMap tmap, unsigne
     c.split(p0 + pl, n, ch);
     return gy + c.y_base(n, ch * m + j);
   };
-  auto issue = [&](int64_t u, T* dst, T* stg, float* tab, uint64_t* bar) {
-    uint32_t grp;
-    const int band = (int)g.d_bands.divmod((uint32_t)u, grp);
-    const int64_t p0 = (int64_t)grp * g.ppc;
-    const int np = (int)((nplanes - p0) < g.ppc ? (nplanes - p0) : g.ppc);
+  auto issue = [&](int64_t p0, int np, int band, T* dst, T* stg, float* tab, uint64_t* bar) {
     // one (plane, j) filter per thread
     for (int sj = threadIdx.x; sj < np * m; sj += kNT) {
       const int pl = m == 1 ? sj : sj / m;
@@ -104,7 +102,10 @@ bwd2_kernel(Conv c, Bwd2Cfg g, const __grid_constant__ CUtensorMap tmap, unsigne
       for (int i = 0; i < K * K; ++i) tab[sj * (K * K) + i] = ld(wp + i);
     }
     if (g.mode == kCopyDense) {
-      issue_flat<T>(stg, np * m, g.seg, [&](int s) { return gy_plane(p0, s); }, (int)(c.Ho * c.Wo));
+      if (g.contig)
+        issue_contig<T>(stg, gy_plane(p0, 0), (int64_t)np * m * c.Ho * c.Wo);
+      else
+        issue_flat<T>(stg, np * m, g.seg, [&](int s) { return gy_plane(p0, s); }, (int)(c.Ho * c.Wo));
       return;
     }
     if (use_tma) {
@@ -121,15 +122,20 @@ bwd2_kernel(Conv c, Bwd2Cfg g, const __grid_constant__ CUtensorMap tmap, unsigne
                   [&](int s) { return gy_plane(p0, s); },
                   (int)c.Ho, (int)c.Wo, band * g.thu + g.row0, g.tr, g.trdiv, g.ix0, g.mode);
   };
-  int64_t u = blockIdx.x;
-  if (u < units) issue(u, buf0, stg0, tab0, &bars[0]);
+  const Sched sch(nplanes, units, g.ppc, g.balanced, g.d_bands);
+  int64_t p0n;
+  int npn, bandn;
+  bool have = sch.stage(0, p0n, npn, bandn);
+  if (have) issue(p0n, npn, bandn, buf0, stg0, tab0, &bars[0]);
   cp_async_commit();
-  for (int k = 0; u < units; ++k, u += gridDim.x) {
+  for (int k = 0; have; ++k) {
+    const int64_t p0 = p0n;
+    const int np = npn, band = bandn;
     T* cur = (k & 1) ? buf1 : buf0;
     const float* tab = (k & 1) ? tab1 : tab0;
-    const bool more = u + gridDim.x < units;
+    const bool more = sch.stage(k + 1, p0n, npn, bandn);
     if (more)
-      issue(u + gridDim.x, (k & 1) ? buf0 : buf1, (k & 1) ? stg0 : stg1, (k & 1) ? tab0 : tab1,
+      issue(p0n, npn, bandn, (k & 1) ? buf0 : buf1, (k & 1) ? stg0 : stg1, (k & 1) ? tab0 : tab1,
             &bars[(k + 1) & 1]);
     cp_async_commit();
     cp_async_wait<1>();
@@ -138,10 +144,6 @@ bwd2_kernel(Conv c, Bwd2Cfg g, const __grid_constant__ CUtensorMap tmap, unsigne
       return;
     }
     __syncthreads();
-    uint32_t grp;
-    const int band = (int)g.d_bands.divmod((uint32_t)u, grp);
-    const int64_t p0 = (int64_t)grp * g.ppc;
-    const int np = (int)((nplanes - p0) < g.ppc ? (nplanes - p0) : g.ppc);
     const int u0 = band * g.thu;  // first u row of the band (gx row S*u0)
     const T* stg = (k & 1) ? stg1 : stg0;
     const bool dense = g.mode == kCopyDense;
@@ -167,7 +169,9 @@ bwd2_kernel(Conv c, Bwd2Cfg g, const __grid_constant__ CUtensorMap tmap, unsigne
         for (int i = 0; i < K * K; ++i) wr[i] = tab[(pl * m + j) * (K * K) + i];
         const T* t = cur + (pl * m + j) * g.tile_elems + (rbi * R) * g.pitch + cbi * V + g.cshift;
         // dense: grad_out plane coordinates of window (0, 0)
-        const T* dp = dense ? dense_plane(stg, g.seg, pl * m + j, gy_plane(p0, pl * m + j)) : nullptr;
+        const T* dp = !dense ? nullptr
+                      : g.contig ? dense_at(stg, gy_plane(p0, 0), (pl * m + j) * (int)(c.Ho * c.Wo))
+                                 : dense_plane(stg, g.seg, pl * m + j, gy_plane(p0, pl * m + j));
         const int gyr = u0 + g.row0 + rbi * R, gyc = g.ix0 + g.cshift + DL + cbi * V;
 #pragma unroll
         for (int ut = 0; ut < R + SP; ++ut) {
@@ -260,6 +264,7 @@ bwd2_kernel(Conv c, Bwd2Cfg g, const __grid_constant__ CUtensorMap tmap, unsigne
       flush_staged<T>(gx + p0 * c.H * c.W, ostg, np * (int)(c.H * c.W), accumulate);
     }
     __syncthreads();
+    have = more;
   }
 }
 
@@ -341,6 +346,8 @@ cudaError_t run_bwd2_t(const Conv& c, const void* gy, const void* w, void* gx, b
   if (tma) g.mode = kCopyTMA;
   g.ppc = (int)ppc;
   g.groups = (nplanes + ppc - 1) / ppc;
+  g.balanced = g.nbands == 1 && g.mode != kCopyTMA;
+  g.contig = g.mode == kCopyDense && c.off == 0 && c.ctot == c.C * c.m;
   g.stage_elems = g.mode == kCopyDense ? 0 : stage_round((int64_t)g.ppc * c.m * g.tile_elems, ES);
   g.tma_bytes = (uint32_t)((int64_t)g.ppc * c.m * g.tile_elems * ES);
   g.stg_elems = g.mode == kCopyDense ? stage_round((int64_t)g.ppc * c.m * g.seg, ES) : 0;

@@ -51,11 +51,7 @@ fwd_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned int
   const int64_t units = g.groups * g.nbands;
   const int64_t HW = c.H * c.W;
   const int nout = g.ppc * c.m;  // output planes per full unit
-  auto issue = [&](int64_t u, T* dst, T* stg, float* tab, uint64_t* bar) {
-    uint32_t grp;
-    const int band = (int)g.d_bands.divmod((uint32_t)u, grp);
-    const int64_t p0 = (int64_t)grp * g.ppc;
-    const int np = (int)((nplanes - p0) < g.ppc ? (nplanes - p0) : g.ppc);
+  auto issue = [&](int64_t p0, int np, int band, T* dst, T* stg, float* tab, uint64_t* bar) {
     if (use_tma) {
       if (threadIdx.x == 0) {
         tma::fence_async_smem();
@@ -63,7 +59,10 @@ fwd_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned int
         tma::load_3d(dst, &tmap, g.ix0, band * g.th * S - c.ph, (int)p0, bar);
       }
     } else if (g.mode == kCopyDense) {
-      issue_flat<T>(stg, np, g.seg, [&](int p) { return x + (p0 + p) * HW; }, (int)HW);
+      if (g.contig)
+        issue_contig<T>(stg, x + p0 * HW, np * HW);
+      else
+        issue_flat<T>(stg, np, g.seg, [&](int p) { return x + (p0 + p) * HW; }, (int)HW);
     } else {
       issue_tile<T>(dst, np, g.tile_elems, g.pitch, [&](int p) { return x + (p0 + p) * HW; },
                     (int)c.H, (int)c.W, band * g.th * S - c.ph, g.tr, g.trdiv, g.ix0, g.mode);
@@ -84,14 +83,19 @@ fwd_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned int
       ot[pj] = c.y_base(n, oc);
     }
   };
-  int64_t u = blockIdx.x;
-  if (u < units) issue(u, buf0, stg0, tab0, &bars[0]);
+  const Sched sch(nplanes, units, g.ppc, g.balanced, g.d_bands);
+  int64_t p0n;
+  int npn, bandn;
+  bool have = sch.stage(0, p0n, npn, bandn);
+  if (have) issue(p0n, npn, bandn, buf0, stg0, tab0, &bars[0]);
   cp_async_commit();
-  for (int k = 0; u < units; ++k, u += gridDim.x) {
+  for (int k = 0; have; ++k) {
+    const int64_t p0 = p0n;
+    const int np = npn, band = bandn;
     T* cur = (k & 1) ? buf1 : buf0;
     const float* tab = (k & 1) ? tab1 : tab0;
-    const bool more = u + gridDim.x < units;
-    if (more) issue(u + gridDim.x, (k & 1) ? buf0 : buf1, (k & 1) ? stg0 : stg1, (k & 1) ? tab0 : tab1,
+    const bool more = sch.stage(k + 1, p0n, npn, bandn);
+    if (more) issue(p0n, npn, bandn, (k & 1) ? buf0 : buf1, (k & 1) ? stg0 : stg1, (k & 1) ? tab0 : tab1,
                     &bars[(k + 1) & 1]);
     cp_async_commit();
     cp_async_wait<1>();
@@ -101,10 +105,6 @@ fwd_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned int
       return;
     }
     __syncthreads();
-    uint32_t grp;
-    const int band = (int)g.d_bands.divmod((uint32_t)u, grp);
-    const int64_t p0 = (int64_t)grp * g.ppc;
-    const int np = (int)((nplanes - p0) < g.ppc ? (nplanes - p0) : g.ppc);
     const T* stg = (k & 1) ? stg1 : stg0;
     const int oh0 = band * g.th;
     const int band_rows = (int)((c.Ho - oh0) < g.th ? (c.Ho - oh0) : g.th);
@@ -133,7 +133,9 @@ fwd_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned int
         for (int v = 0; v < V; ++v) acc[r][v] = bv;
       if (g.mode == kCopyDense) {
         const int pl = pj / c.m;
-        conv_block_dense<K, S, D, R, V, Q>(dense_plane(stg, g.seg, pl, x + (p0 + pl) * HW), (int)c.H, (int)c.W,
+        const T* dp = g.contig ? dense_at(stg, x + p0 * HW, pl * (int)HW)
+                               : dense_plane(stg, g.seg, pl, x + (p0 + pl) * HW);
+        conv_block_dense<K, S, D, R, V, Q>(dp, (int)c.H, (int)c.W,
                                            ohr * S - c.ph, owb * S - c.pw, wr, acc);
       } else {
         conv_block<K, S, D, R, V, Q, DL>(cur + (pj / c.m) * g.tile_elems, g.pitch, ohr * S, owb * S + g.cshift, wr, acc);
@@ -142,6 +144,7 @@ fwd_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned int
                               g.vec_out, false);
     }
     __syncthreads();
+    have = more;
   }
 }
 
@@ -177,14 +180,13 @@ bwd1_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned in
     c.split(p0 + pl, n, ch);
     return gy + c.y_base(n, ch * m + j);
   };
-  auto issue = [&](int64_t u, T* dst, T* stg, float* tab, uint64_t* bar) {
-    uint32_t grp;
-    const int band = (int)g.d_bands.divmod((uint32_t)u, grp);
-    const int64_t p0 = (int64_t)grp * g.ppc;
-    const int np = (int)((nplanes - p0) < g.ppc ? (nplanes - p0) : g.ppc);
+  auto issue = [&](int64_t p0, int np, int band, T* dst, T* stg, float* tab, uint64_t* bar) {
     // staged plane s = pl * m + j holds gy[n, off + c*m + j]
     if (g.mode == kCopyDense) {
-      issue_flat<T>(stg, np * m, g.seg, [&](int s) { return gy_plane(p0, s); }, (int)(c.Ho * c.Wo));
+      if (g.contig)
+        issue_contig<T>(stg, gy_plane(p0, 0), (int64_t)np * m * c.Ho * c.Wo);
+      else
+        issue_flat<T>(stg, np * m, g.seg, [&](int s) { return gy_plane(p0, s); }, (int)(c.Ho * c.Wo));
     } else if (use_tma) {
       if (threadIdx.x == 0) {
         int64_t n, ch;
@@ -210,14 +212,19 @@ bwd1_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned in
     }
     for (int pl = threadIdx.x; pl < np; pl += kNT) ot[pl] = (p0 + pl) * c.H * c.W;
   };
-  int64_t u = blockIdx.x;
-  if (u < units) issue(u, buf0, stg0, tab0, &bars[0]);
+  const Sched sch(nplanes, units, g.ppc, g.balanced, g.d_bands);
+  int64_t p0n;
+  int npn, bandn;
+  bool have = sch.stage(0, p0n, npn, bandn);
+  if (have) issue(p0n, npn, bandn, buf0, stg0, tab0, &bars[0]);
   cp_async_commit();
-  for (int k = 0; u < units; ++k, u += gridDim.x) {
+  for (int k = 0; have; ++k) {
+    const int64_t p0 = p0n;
+    const int np = npn, band = bandn;
     T* cur = (k & 1) ? buf1 : buf0;
     const float* tab = (k & 1) ? tab1 : tab0;
-    const bool more = u + gridDim.x < units;
-    if (more) issue(u + gridDim.x, (k & 1) ? buf0 : buf1, (k & 1) ? stg0 : stg1, (k & 1) ? tab0 : tab1,
+    const bool more = sch.stage(k + 1, p0n, npn, bandn);
+    if (more) issue(p0n, npn, bandn, (k & 1) ? buf0 : buf1, (k & 1) ? stg0 : stg1, (k & 1) ? tab0 : tab1,
                     &bars[(k + 1) & 1]);
     cp_async_commit();
     cp_async_wait<1>();
@@ -226,10 +233,6 @@ bwd1_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned in
       return;
     }
     __syncthreads();
-    uint32_t grp;
-    const int band = (int)g.d_bands.divmod((uint32_t)u, grp);
-    const int64_t p0 = (int64_t)grp * g.ppc;
-    const int np = (int)((nplanes - p0) < g.ppc ? (nplanes - p0) : g.ppc);
     const T* stg = (k & 1) ? stg1 : stg0;
     const int ih0 = band * g.th;
     const int band_rows = (int)((c.H - ih0) < g.th ? (c.H - ih0) : g.th);
@@ -256,7 +259,9 @@ bwd1_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned in
         for (int i = 0; i < K * K; ++i) wr[i] = tab[(pl * m + j) * (K * K) + i];
         if (g.mode == kCopyDense) {
           const int sp = pl * m + j;
-          conv_block_dense<K, 1, D, R, V, Q>(dense_plane(stg, g.seg, sp, gy_plane(p0, sp)), (int)c.Ho,
+          const T* dp = g.contig ? dense_at(stg, gy_plane(p0, 0), sp * (int)(c.Ho * c.Wo))
+                                 : dense_plane(stg, g.seg, sp, gy_plane(p0, sp));
+          conv_block_dense<K, 1, D, R, V, Q>(dp, (int)c.Ho,
                                              (int)c.Wo, ihr - qh, iwb - (D * (K - 1) - c.pw), wr, acc);
         } else {
           conv_block<K, 1, D, R, V, Q, DL>(cur + (pl * m + j) * g.tile_elems, g.pitch, ihr, iwb + g.cshift, wr, acc);
@@ -266,6 +271,7 @@ bwd1_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned in
                               g.vec_out, accumulate);
     }
     __syncthreads();
+    have = more;
   }
 }
 
@@ -296,6 +302,7 @@ cudaError_t run_fwd_t(const Conv& c, const void* x, const void* w, const void* b
   if (!plan_tile<T, K, S, D, R, V>(c.N * c.C, 1, c.m, c.H, c.W, c.Ho, c.Wo, c.pw, x, vout, &g, &dl, 0,
                                    c.N * c.C, &map))
     return cudaErrorInvalidConfiguration;
+  g.contig = g.mode == kCopyDense;  // x planes n*C + c are contiguous
 
   switch (dl) {
     case 0: return launch_fwd<T, K, S, D, 0>(c, g, map, x, w, b, y, s);
@@ -332,6 +339,8 @@ cudaError_t run_bwd1_t(const Conv& c, const void* gy, const void* w, void* gx, b
   if (!plan_tile<T, K, 1, D, R, V>(c.N * c.C, c.m, 1, c.Ho, c.Wo, c.H, c.W, qw, gy, vout, &g, &dl, c.C,
                                    c.N * c.ctot, &map))
     return cudaErrorInvalidConfiguration;
+  // grad_out planes of consecutive (n, c) are contiguous without a channel slice
+  g.contig = g.mode == kCopyDense && c.off == 0 && c.ctot == c.C * c.m;
 
   switch (dl) {
     case 0: return launch_bwd1<T, K, D, 0>(c, g, map, qh, gy, w, gx, acc, s);

@@ -28,6 +28,8 @@ struct Cfg {
   uint32_t tma_bytes;  // bytes one stage's tensor copy delivers
   int seg;             // dense staging: elements per plane segment
   int stg_elems;       // dense staging: elements per stage (0 otherwise)
+  int balanced;        // equal contiguous plane shares per CTA (see Sched)
+  int contig;          // dense staging: a stage's planes are one contiguous run
 };
 
 
@@ -122,6 +124,7 @@ bool plan_tile(int64_t nplanes, int ntile, int mult, int64_t Hin, int64_t Win, i
   if (tma) g.mode = kCopyTMA;
   g.ppc = (int)ppc;
   g.groups = (nplanes + ppc - 1) / ppc;
+  g.balanced = g.nbands == 1 && g.mode != kCopyTMA;
   g.stage_elems = g.mode == kCopyDense ? 0 : stage_round((int64_t)g.ppc * ntile * g.tile_elems, ES);
   g.tma_bytes = (uint32_t)((int64_t)g.ppc * ntile * g.tile_elems * ES);
   g.stg_elems = g.mode == kCopyDense ? stage_round((int64_t)g.ppc * ntile * g.seg, ES) : 0;
