@@ -30,12 +30,14 @@ const char* algo_name(Algo a) {
     case Algo::Tile: return "tile";
     case Algo::Large: return "large";
     case Algo::IBGemm: return "ibgemm";
+    case Algo::Plane: return "plane";
   }
   return "unknown";
 }
 
 Algo plan_fwd(const Conv& c) {
   if (force_generic()) return Algo::Generic;
+  if (plane::fwd_supported(c)) return Algo::Plane;
   if (tile::fwd_supported(c)) return Algo::Tile;
   if (allow_ibgemm() && ibg::fwd_supported(c)) return Algo::IBGemm;
   if (large::supported(c)) return Algo::Large;
@@ -44,6 +46,7 @@ Algo plan_fwd(const Conv& c) {
 
 Algo plan_bwd_data(const Conv& c) {
   if (force_generic()) return Algo::Generic;
+  if (plane::bwd_data_supported(c)) return Algo::Plane;
   if (c.sh == 1 ? tile::bwd1_supported(c) : tile::bwd2_supported(c)) return Algo::Tile;
   if (allow_ibgemm() && ibg::bwd_data_supported(c)) return Algo::IBGemm;
   if (large::supported(c)) return Algo::Large;
@@ -51,6 +54,7 @@ Algo plan_bwd_data(const Conv& c) {
 }
 
 WPlan plan_bwd_weight(const Conv& c) {
+  if (!force_generic() && plane::wgrad_supported(c)) return WPlan{Algo::Plane, plane::wgrad_chunks(c)};
   if (!force_generic() && tile::wgrad_supported(c)) return WPlan{Algo::Tile, tile::wgrad_chunks(c)};
   if (!force_generic() && large::supported(c)) return WPlan{Algo::Large, large::wgrad_chunks(c)};
   // generic first pass: a chunk of whole samples per block, at most 2^20
@@ -67,6 +71,7 @@ WPlan plan_bwd_weight(const Conv& c) {
 cudaError_t run_fwd(Algo a, const Conv& c, const void* x, const void* w, const void* b, void* y,
                     cudaStream_t s) {
   switch (a) {
+    case Algo::Plane: return plane::fwd(c, x, w, b, y, s);
     case Algo::Tile: return tile::fwd(c, x, w, b, y, s);
     case Algo::Large: return large::fwd(c, x, w, b, y, s);
     case Algo::IBGemm: {
@@ -82,6 +87,7 @@ cudaError_t run_fwd(Algo a, const Conv& c, const void* x, const void* w, const v
 cudaError_t run_bwd_data(Algo a, const Conv& c, const void* gy, const void* w, void* gx,
                          bool accumulate, cudaStream_t s) {
   switch (a) {
+    case Algo::Plane: return plane::bwd_data(c, gy, w, gx, accumulate, s);
     case Algo::Tile:
       return c.sh == 1 ? tile::bwd1(c, gy, w, gx, accumulate, s) : tile::bwd2(c, gy, w, gx, accumulate, s);
     case Algo::Large: return large::bwd_data(c, gy, w, gx, accumulate, s);
@@ -99,6 +105,9 @@ cudaError_t run_bwd_weight(const WPlan& p, const Conv& c, const void* x, const v
                            void* gb, float* ws, cudaStream_t s) {
   cudaError_t e;
   switch (p.algo) {
+    case Algo::Plane:
+      e = plane::wgrad(c, x, gy, ws, p.chunks, s);
+      break;
     case Algo::Tile:
       e = tile::wgrad(c, x, gy, ws, p.chunks, s);
       break;

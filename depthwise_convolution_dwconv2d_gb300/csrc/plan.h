@@ -12,6 +12,7 @@ enum class Algo {
   Tile = 1,      // tile_fwd.cu / tile_bwd.cu: register-blocked smem tiles, small kernels
   Large = 2,     // large.cu: large-kernel direct convolution
   IBGemm = 3,    // ibgemm.cu: large-kernel implicit batched GEMM on tcgen05 (fp16 / bf16)
+  Plane = 4,     // plane.cu: 3x3 on small planes, one warp per group of whole planes
 };
 
 struct WPlan {
@@ -67,6 +68,19 @@ cudaError_t bwd_data(const Conv& c, const void* gy, const void* w, void* gx, boo
 int wgrad_chunks(const Conv& c);
 cudaError_t wgrad(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s);
 }  // namespace large
+
+namespace plane {
+// plane.cu: 3x3 on small planes (fwd: rows of 9..16; grad-input: stride 1 and rows
+// of 9..16; weight gradient: output rows of at most 16)
+bool fwd_supported(const Conv& c);
+bool bwd_data_supported(const Conv& c);
+bool wgrad_supported(const Conv& c);
+int wgrad_chunks(const Conv& c);
+int64_t wgrad_nb(const Conv& c);  // samples per chunk (chunks = ceil(N / wgrad_nb))
+cudaError_t fwd(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s);
+cudaError_t bwd_data(const Conv& c, const void* gy, const void* w, void* gx, bool acc, cudaStream_t s);
+cudaError_t wgrad(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s);
+}  // namespace plane
 
 namespace ibg {
 // ibgemm.cu: tensor-core implicit batched GEMM, stride 1, 16-bit data

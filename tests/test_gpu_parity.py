@@ -403,3 +403,65 @@ def test_ibgemm_misaligned_input_falls_back():
 
 def test_no_bounded_wait_gave_up_after_ibgemm():
     assert B.dwconv_device_timeouts() == 0
+
+
+# ------------------------------------------------------ small-plane kernels
+PLANE_CASES = [
+    WL.Layer(N=3, C=5, H=14, W=14, k=3, s=1, p=1, bias=True, dtype="f32"),
+    WL.Layer(N=5, C=3, H=15, W=13, k=3, s=2, p=1, dtype="f32"),
+    WL.Layer(N=2, C=4, H=7, W=7, k=3, s=2, p=1, dtype="bf16"),
+    WL.Layer(N=3, C=2, H=28, W=28, k=3, s=2, p=1, bias=True, dtype="f16"),
+    WL.Layer(N=2, C=3, H=9, W=16, k=3, s=1, p=0, dtype="f32"),
+    WL.Layer(N=2, C=3, H=10, W=11, k=3, s=1, p=2, dtype="f32"),
+    WL.Layer(N=17, C=3, H=10, W=11, k=3, s=2, p=2, bias=True, dtype="f32"),
+]
+PLANE_IDS = ["14s1", "15x13s2", "7s2bf16", "28s2f16", "w16p0", "p2s1", "p2s2N17"]
+
+
+@pytest.mark.parametrize("L", PLANE_CASES, ids=PLANE_IDS)
+def test_plane_kernels_vs_oracle(L):
+    """One warp per group of small planes: odd sizes, stride 2, padding 0 and
+    2, ragged batches, all dtypes, bias. The planner uses them for the forward
+    on rows of 9..16, the stride-1 grad-input on rows of 9..16 and the
+    weight gradient on output rows of at most 16."""
+    d = desc_of(L)
+    narrow = 8 < L.W <= 16
+    assert (B.dwconv2d_plan_name(d, 0) == "plane") == narrow
+    assert (B.dwconv2d_plan_name(d, 1) == "plane") == (narrow and L.s == 1)
+    assert B.dwconv2d_plan_name(d, 2) == "plane"
+    check_full(L, WL.make_inputs(L), L.label())
+
+
+@pytest.mark.parametrize("L", [PLANE_CASES[0], PLANE_CASES[1]], ids=PLANE_IDS[:2])
+def test_plane_slices_and_accumulate(L):
+    """Output slice written in place, grad_out read from the slice, grad-input accumulates."""
+    th = torch()
+    inp = WL.make_inputs(L, gy_channels=L.OC + 4)
+    ctot, off = L.OC + 4, 2
+    d = desc_of(L, off, ctot)
+    assert B.dwconv2d_plan_name(d, 0) == "plane"
+    x, w = to_dev(inp.x), to_dev(inp.w)
+    b = to_dev(inp.b) if inp.b is not None else None
+    y = empty_dev((L.N, ctot, L.Ho, L.Wo), L.dtype, fill=-3.0)
+    B.dwconv2d_fwd(d, x, w, b, y)
+    yh = to_f64(y)
+    assert np.all(yh[:, :off] == -3.0) and np.all(yh[:, off + L.OC:] == -3.0)
+    cv = oconv(L, off=off, c_total=ctot)
+    ry = oracle.fwd(cv, inp.x.f64, inp.w.f64, inp.b.f64 if inp.b is not None else None)
+    assert_close(yh[:, off:off + L.OC], ry[:, off:off + L.OC], L.dtype, 9, "plane slice fwd")
+    gy = to_dev(inp.gy)
+    gx = empty_dev((L.N, L.C, L.H, L.W), L.dtype, fill=0.25)
+    B.dwconv2d_bwd_data(d, gy, w, gx, 1)
+    th.cuda.synchronize()
+    rgx = oracle.bwd_data(cv, inp.gy.f64, inp.w.f64) + 0.25
+    assert_close(to_f64(gx), rgx, L.dtype, 9, "plane accumulate bwd_data")
+    gw = empty_dev((L.OC, L.k, L.k), L.dtype)
+    ws, nb = ws_for(d)
+    B.dwconv2d_bwd_weight(d, x, gy, gw, None, ws, nb)
+    th.cuda.synchronize()
+    rgw, _ = oracle.bwd_weight(cv, inp.x.f64, inp.gy.f64)
+    assert_close(to_f64(gw), rgw, L.dtype, 9, "plane slice bwd_weight")
+
+
+def test_no_bounded_wait_gave_up_at_end():
+    assert B.dwconv_device_timeouts() == 0
