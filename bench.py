@@ -516,7 +516,9 @@ def gpu_arm(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 300 for the MobileNet sweep, so the timed region spans "
+                         "several clock samples; 20 otherwise and for the reference arm)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="mobilenet", choices=sorted(WORKLOAD_TEXT))
@@ -527,6 +529,8 @@ def main():
     ap.add_argument("--layers", default="", help="comma-separated layer labels to keep (profiling runs)")
     ap.add_argument("--batch", type=int, default=0, help="override the batch size (profiling runs)")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = 300 if (args.workload == "mobilenet" and args.impl == "gb300") else 20
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
 
