@@ -110,8 +110,7 @@ __device__ __forceinline__ void issue_tile(T* __restrict__ dst, int np, int plan
 // cp.async chunks into a staging segment of `seg` elements, starting at the
 // plane's own offset within its 16-byte chunk (its address mod 16); the last
 // chunk is cut at the plane's end by the copy's source size, so nothing
-// outside the plane's 16-byte neighbourhood is read. repitch() then moves the
-// samples into the padded tile layout.
+// outside the plane's 16-byte neighbourhood is read.
 template <typename T, typename SrcOf>
 __device__ __forceinline__ void issue_flat(T* __restrict__ stg, int np, int seg, SrcOf src_of, int HW) {
   constexpr int ES = sizeof(T);
@@ -152,30 +151,6 @@ __device__ __forceinline__ const T* dense_at(const T* stg, const T* src0, int of
   return stg + (int)((reinterpret_cast<uintptr_t>(src0) & 15) / sizeof(T)) + off;
 }
 
-template <typename T, typename SrcOf>
-__device__ __forceinline__ void repitch(T* __restrict__ dst, int np, int plane_elems, int pitch,
-                                        const T* __restrict__ stg, int seg, SrcOf src_of, int H, int W,
-                                        int iy0, int tr, const FastDiv& trdiv, int ix0) {
-  constexpr int ES = sizeof(T);
-  const int lpr = pitch > 16 ? 32 : pitch > 8 ? 16 : pitch > 4 ? 8 : 4;
-  const int rpw = 32 / lpr;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int sub = lane / lpr, l = lane & (lpr - 1);
-  const int nwarps = blockDim.x >> 5;
-  for (int q = warp * rpw + sub; q < np * tr; q += nwarps * rpw) {
-    uint32_t p;
-    const int r = (int)trdiv.divmod((uint32_t)q, p);
-    const int iy = iy0 + r;
-    const bool rin = iy >= 0 && iy < H;
-    const int mo = (int)((reinterpret_cast<uintptr_t>(src_of((int)p)) & 15) / ES);
-    const T* srow = stg + (int)p * seg + mo + (rin ? iy : 0) * W;
-    T* drow = dst + (int)p * plane_elems + r * pitch;
-    for (int c = l; c < pitch; c += lpr) {
-      const int ix = ix0 + c;
-      drow[c] = (rin && ix >= 0 && ix < W) ? srow[ix] : from_f<T>(0.f);
-    }
-  }
-}
 
 // Segment size (elements) of one densely staged plane: room for the
 // in-chunk offset and the rounding of the last chunk.

@@ -172,7 +172,8 @@ dwconv_status_t dwconv2d_bwd_data_multi(int nbranch, const dwconv2d_desc_t* desc
 const char* dwconv_status_string(dwconv_status_t status);
 
 /* Name of the kernel family the planner picks for a pass (0 = fwd,
- * 1 = bwd_data, 2 = bwd_weight) of this descriptor: "tile" (small filters),
+ * 1 = bwd_data, 2 = bwd_weight) of this descriptor: "plane" (3x3 on small
+ * planes, one warp per group of whole planes), "tile" (small filters),
  * "large" (large-filter direct convolution), "ibgemm" (large-filter fp16 /
  * bf16 forward and grad-input as an implicit batched GEMM on the tensor
  * cores), "generic" (any shape) or "invalid". Host only; for logs and tests.
