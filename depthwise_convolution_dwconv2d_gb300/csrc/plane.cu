@@ -5,23 +5,34 @@
 // output per thread straight from global memory; the tile kernels stage bands
 // of many planes per CTA. For the small MobileNet planes (7², 14², 28²) both
 // spend most of their instructions on indexing and staging, so here a warp
-// works alone on a few whole planes:
-//  * it copies the planes (coalesced, row by row) into its own zero-haloed
-//    tile in shared memory -- no CTA barrier, no staging pipeline; latency
-//    is hidden by the many warps resident on an SM;
+// works alone on a few whole planes of one channel (P samples at a time):
+//  * it copies the planes (coalesced rows, 8-byte granules where aligned)
+//    into its own zero-haloed tile in shared memory, together with what the
+//    compute needs next to them (the channel's filter taps and bias; for the
+//    weight gradient the grad_out planes), all with asynchronous copies
+//    issued one work item ahead -- no CTA barrier and no global load on the
+//    compute path;
 //  * each lane owns one output column of one plane (two or four planes per
 //    warp when the planes are narrow) and walks the output rows with the
 //    K x K window held in registers (a stride-1 step loads one new row of
-//    K values), so an output costs K loads, K*K FMAs and a store, with no
-//    bounds checks.
+//    K values), so an output costs K shared loads, K*K FMAs and a store;
+//    the walk is unrolled (fully for the common plane heights), with 32-bit
+//    shared offsets and running pointers, so almost no integer work is left
+//    per output row.
 // The same correlation kernel serves the forward and the stride-1
 // grad-input (grad_out correlated with the filter rotated by 180 degrees,
-// padding K-1-p); the weight-gradient first pass accumulates K*K + 1 sums
-// per lane and reduces them in a fixed order into one partial per
-// (chunk, channel). Measured against the tile kernels on the MobileNet
-// layers, these win for the forward and stride-1 grad-input on rows of
-// 9..16 elements and for the weight gradient on output rows of at most 16;
-// the planner uses them there only.
+// padding K-1-p). In the weight-gradient first pass each warp owns whole
+// (chunk, channel) units: its lanes accumulate K*K + 1 sums over the unit's
+// sample groups, and at the end of a unit a butterfly reduces them into the
+// unit's partial; the walk (and its copies) runs on across unit boundaries.
+// Measured against the tile kernels on the MobileNet layers, these win for
+// the forward and stride-1 grad-input on rows of 9..16 elements and for the
+// weight gradient on output rows of at most 16; the planner uses them there
+// only.
+#include <algorithm>
+#include <cstdint>
+#include <type_traits>
+
 #include "plan.h"
 #include "tile.cuh"
 
@@ -29,18 +40,26 @@ namespace dwconv {
 namespace plane {
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 8;  // warps per CTA of the correlation kernels
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxW = 32;  // widest input / output row (one lane per column)
+constexpr int kRB = 16;    // output rows per unrolled block of a lane's walk
+constexpr int kCO = 2;     // tile column of input column 0 (even: 8-byte copies land aligned)
 
 struct PCfg {
   int Hin, Win, Hout, Wout;  // planes read / written
   int pad;                   // padding of the evaluated correlation
   int L, P;                  // lanes per plane (power of two >= output columns), planes per warp (32 / L)
-  int Lw;                    // lanes per row when loading (power of two >= Win, <= 32)
-  int TR, TP, TS;            // tile rows, pitch and floats per plane
-  int64_t nplanes, groups;   // planes, groups of P planes
-  int nb;                    // weight gradient: samples per chunk
+  int gran;                  // floats per plane copy granule: 2 (8-byte fp32 copies) or 1
+  int ggran;                 // floats per grad_out copy granule (weight gradient): 4 (16-byte) or 1
+  int Lw;                    // lanes per row when copying (power of two >= granules per row)
+  int TR, TP, TS;            // tile rows, pitch (even), floats per plane slot
+  int GS;                    // weight gradient: floats per staged grad_out plane slot
+  int XO;                    // floats of a buffer before its filter taps / grad_out planes
+  int BS;                    // floats per tile buffer (two per warp; a multiple of 4)
+  int gpc;                   // sample groups per channel (ceil(N / P))
+  int nb, G;                 // weight gradient: samples per chunk, sample groups per chunk
+  int klast;                 // weight gradient: group holding the last chunk's last sample
 };
 
 int pow2_at_least(int v) {
@@ -49,207 +68,330 @@ int pow2_at_least(int v) {
   return p;
 }
 
-// Copy plane rows (Hin x Win, from src) into a tile whose element (r, col) is
-// source (r - off, col - off), keeping only the tile's TR x TP window.
-__device__ __forceinline__ void load_rows_setup(const PCfg& g, int lane, int& lr, int& lc, int& rstep) {
-  lr = lane / g.Lw;
-  lc = lane - lr * g.Lw;
-  rstep = 32 / g.Lw;
+// smallest v' >= v with v' = r (mod 32)
+int round_to_residue(int v, int r) {
+  r &= 31;
+  return v + ((r - v) % 32 + 32) % 32;
 }
 
-// fp32 planes are copied with 4-byte asynchronous copies (all in flight at
-// once, completed by the caller's cp_async_wait); 16-bit planes are widened
-// through registers.
-template <typename T>
-__device__ __forceinline__ void load_plane(float* __restrict__ dst, const T* __restrict__ src, const PCfg& g,
-                                           int off, int lr, int lc, int rstep) {
-  if (lc >= g.Win || lc + off >= g.TP) return;
-  int rend = g.TR - off;
-  if (rend > g.Hin) rend = g.Hin;
-  if (sizeof(T) == 4) {
-    for (int r = lr; r < rend; r += rstep)
-      tile::cp_async4(dst + (r + off) * g.TP + lc + off, src + r * g.Win + lc, 4);
-  } else {
-#pragma unroll 4
-    for (int r = lr; r < rend; r += rstep) dst[(r + off) * g.TP + lc + off] = ld(src + r * g.Win + lc);
+// asynchronous copies to a 32-bit shared-memory byte address
+__device__ __forceinline__ void cp4(uint32_t s, const void* g) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, 4;\n" ::"r"(s), "l"(g) : "memory");
+}
+__device__ __forceinline__ void cp8(uint32_t s, const void* g) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, 8;\n" ::"r"(s), "l"(g) : "memory");
+}
+__device__ __forceinline__ void cp16(uint32_t s, const void* g) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, 16;\n" ::"r"(s), "l"(g) : "memory");
+}
+
+// Copies of a group of np <= P planes into tile slots slot0 + q*TS: plane q
+// is read at src0 + q*pstride (rows Win elements apart); its input row r
+// lands on tile row r + pad and input column j on tile column kCO + j; the
+// rest of a slot (the zero halo) is never written. The warp walks the
+// group's rows flattened over the planes: lane (lr, lc) copies granule lc of
+// rows lr, lr + rstep, ..., advancing its (plane, row) cursor by a constant
+// step (no per-plane setup, no division). fp32 goes by asynchronous copies
+// (completed by the caller's wait), 16-bit types are widened through
+// registers.
+struct RowCopier {
+  int lr, lc, rstep;  // lane's first row and granule, rows per warp step
+  int q0, r0;         // lr as (plane, row)
+  int dq, dr;         // rstep as (planes, rows)
+  __device__ RowCopier(const PCfg& g, int lane) {
+    lr = lane / g.Lw;
+    lc = lane - lr * g.Lw;
+    rstep = 32 / g.Lw;
+    q0 = lr / g.Hin;
+    r0 = lr - q0 * g.Hin;
+    dq = rstep / g.Hin;
+    dr = rstep - dq * g.Hin;
   }
+  template <typename T>
+  __device__ __forceinline__ void run(float* psm, int slot0, const T* __restrict__ src0, int64_t pstride, int np,
+                                      const PCfg& g) const {
+    const int cw = (sizeof(T) == 4 ? g.gran : 1) * lc;
+    if (cw >= g.Win) return;
+    const int rend = min(g.Hin, g.TR - g.pad);
+    int q = q0, r = r0;
+    int di = slot0 + q * g.TS + (r + g.pad) * g.TP + kCO + cw;
+    const T* sp = src0 + q * pstride + r * g.Win + cw;
+    const int dstep = dq * g.TS + dr * g.TP, dwrap = g.TS - g.Hin * g.TP;
+    const int64_t sstep = dq * pstride + dr * g.Win, swrap = pstride - (int64_t)g.Hin * g.Win;
+    const uint32_t sb = (uint32_t)__cvta_generic_to_shared(psm);
+    while (q < np) {
+      if (r < rend) {
+        if (sizeof(T) != 4) psm[di] = ld(sp);
+        else if (g.gran == 2) cp8(sb + 4u * di, sp);
+        else cp4(sb + 4u * di, sp);
+      }
+      r += dr;
+      q += dq;
+      di += dstep;
+      sp += sstep;
+      if (r >= g.Hin) {
+        r -= g.Hin;
+        ++q;
+        di += dwrap;
+        sp += swrap;
+      }
+    }
+  }
+};
+
+// Zero a warp's two tile buffers (2 * BS floats from float index b0, a
+// multiple of 4) with 16-byte stores.
+__device__ __forceinline__ void zero_buffers(float* psm, int b0, int BS, int lane) {
+  float4* z = reinterpret_cast<float4*>(psm + b0);
+  for (int i = lane; i < BS / 2; i += 32) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  __syncwarp();
 }
 
-// One warp's walk over work items first, first + step, ...: item k+1 is
-// copied into the other tile buffer while item k is computed.
+// One warp's run over its work items [ia, ib): item i+1 is copied into the
+// other tile buffer while item i is computed. issue(buf) and compute(buf)
+// are called once per item, in item order (each keeps its own cursor).
 template <typename Issue, typename Compute>
-__device__ __forceinline__ void warp_walk(int64_t first, int64_t step, int64_t end, float* buf0, float* buf1,
-                                          Issue issue, Compute compute) {
-  if (first < end) issue(first, buf0);
+__device__ __forceinline__ void warp_run(int ia, int ib, int buf0, int buf1, Issue issue, Compute compute) {
+  if (ia < ib) issue(buf0);
   tile::cp_async_commit();
-  int k = 0;
-  for (int64_t it = first; it < end; it += step, ++k) {
-    const int64_t nx = it + step;
-    if (nx < end) issue(nx, (k & 1) ? buf0 : buf1);
+  for (int it = ia; it < ib; ++it) {
+    const int cur = ((it - ia) & 1) ? buf1 : buf0;
+    if (it + 1 < ib) issue(cur == buf0 ? buf1 : buf0);
     tile::cp_async_commit();
     tile::cp_async_wait<1>();
     __syncwarp();
-    compute(it, (k & 1) ? buf1 : buf0);
+    compute(cur);
     __syncwarp();
   }
   tile::cp_async_wait<0>();
 }
 
-// out[oy][ox] = bias + sum_{a,b} w'[a][b] in[oy*S - pad + a][ox*S - pad + b]
-// MODE 0: forward (in = x, whose planes n*C + c are contiguous; out = y slice)
-// MODE 1: stride-1 grad-input (in = grad_out slice, w' = rot180(w), out = gx)
-template <typename T, int K, int S, int MODE>
-__global__ void __launch_bounds__(kThreads)
-conv_kernel(Conv c, PCfg g, const T* __restrict__ in, const T* __restrict__ w, const T* __restrict__ bias,
-            T* __restrict__ out, int accumulate) {
-  extern __shared__ __align__(16) float psm[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* const buf0 = psm + warp * 2 * g.P * g.TS;
-  float* const buf1 = buf0 + g.P * g.TS;
-  for (int i = lane; i < 2 * g.P * g.TS; i += 32) buf0[i] = 0.f;  // the halo stays zero
-  __syncwarp();
-  const int pl = lane / g.L, ox = lane - pl * g.L;
-  int lr, lc, rstep;
-  load_rows_setup(g, lane, lr, lc, rstep);
-  const int64_t hw_in = (int64_t)g.Hin * g.Win, hw_out = (int64_t)g.Hout * g.Wout;
-  auto issue = [&](int64_t grp, float* tile) {
-    const int64_t p0 = grp * g.P;
-    for (int q = 0; q < g.P; ++q) {
-      const int64_t pin = p0 + q;
-      if (pin >= g.nplanes) break;
-      const T* src;
-      if (MODE == 0) {
-        src = in + pin * hw_in;
-      } else {
-        int64_t n, ch;
-        c.split(pin, n, ch);
-        src = in + c.y_base(n, ch);
-      }
-      load_plane<T>(tile + q * g.TS, src, g, g.pad, lr, lc, rstep);
-    }
-  };
-  auto compute = [&](int64_t grp, const float* tile) {
-    const int64_t pin = grp * g.P + pl;
-    if (ox >= g.Wout || pin >= g.nplanes) return;
-    int64_t n, ch;
-    c.split(pin, n, ch);
-    float wr[K * K];
+// A lane's walk down its output column. t0 is the shared-memory float index
+// of its window's top-left element for output row 0 (tile rows TP floats
+// apart); row(win) is called for output rows 0, 1, ... in order with the
+// K x K window. Addresses are 32-bit shared offsets advanced by constant
+// strides, and the window's row shifts are register renames: rows run fully
+// unrolled when the height HB is a compile-time constant, else in unrolled
+// blocks of kRB with a bound check per row.
+template <int K, int S, int HB, typename Row>
+__device__ __forceinline__ void walk_rows(const float* __restrict__ sm, int t0, int TP, int Hout, Row row) {
+  float win[K][K];
 #pragma unroll
-    for (int i = 0; i < K * K; ++i) wr[i] = ld(w + ch * (K * K) + (MODE == 1 ? K * K - 1 - i : i));
-    const float bv = (MODE == 0 && bias) ? ld(bias + ch) : 0.f;
-    T* dst = MODE == 0 ? out + c.y_base(n, ch) : out + pin * hw_out;
-    const float* tp = tile + pl * g.TS + ox * S;
-    // window rows oy*S + a; a step of one output row drops the first S rows
-    float win[K][K];
+  for (int a = 0; a < K - S; ++a)
+#pragma unroll
+    for (int b = 0; b < K; ++b) win[a + S][b] = sm[t0 + a * TP + b];
+  int t = t0 + (K - S) * TP;  // first tile row not yet in the window
+  auto step = [&]() {
 #pragma unroll
     for (int a = 0; a < K - S; ++a)
 #pragma unroll
-      for (int b = 0; b < K; ++b) win[a + S][b] = tp[a * g.TP + b];
-    for (int oy = 0; oy < g.Hout; ++oy) {
+      for (int b = 0; b < K; ++b) win[a][b] = win[a + S][b];
 #pragma unroll
-      for (int a = 0; a < K - S; ++a)
+    for (int a = K - S; a < K; ++a)
 #pragma unroll
-        for (int b = 0; b < K; ++b) win[a][b] = win[a + S][b];
-      const float* rowp = tp + oy * S * g.TP;
+      for (int b = 0; b < K; ++b) win[a][b] = sm[t + (a - (K - S)) * TP + b];
+    t += S * TP;
+    row(win);
+  };
+  if (HB > 0) {
 #pragma unroll
-      for (int a = K - S; a < K; ++a)
+    for (int oy = 0; oy < HB; ++oy) step();
+  } else {
+    for (int ob = 0; ob < Hout; ob += kRB) {
 #pragma unroll
-        for (int b = 0; b < K; ++b) win[a][b] = rowp[a * g.TP + b];
+      for (int u = 0; u < kRB; ++u) {
+        if (ob + u >= Hout) break;
+        step();
+      }
+    }
+  }
+}
+
+// Cursor over (channel, index within channel) with a fixed count per channel.
+struct Cursor {
+  int ch, j;
+  __device__ __forceinline__ void next(int per) {
+    if (++j == per) {
+      j = 0;
+      ++ch;
+    }
+  }
+};
+
+// out[oy][ox] = bias + sum_{a,b} w'[a][b] in[oy*S - pad + a][ox*S - pad + b]
+// MODE 0: forward (in = x, out = y slice)
+// MODE 1: stride-1 grad-input (in = grad_out slice, w' = rot180(w), out = gx;
+//         ACC adds to gx instead of overwriting it)
+// Work item i = (channel ch, sample group k): the planes (n, ch) for n in
+// [k*P, k*P + P), channel-major, so a warp's consecutive items share their
+// filter. A tile buffer holds the group's P plane slots (TS floats each) and
+// then the channel's K*K filter taps and bias (zero when absent). Global warp
+// w runs items [I*w/Wt, I*(w+1)/Wt) of the I = C * gpc items. HB > 0: every
+// output plane has HB rows.
+template <typename T, int K, int S, int MODE, bool ACC, int HB>
+__global__ void __launch_bounds__(kThreads, 4)
+conv_kernel(Conv c, PCfg g, const T* __restrict__ in, const T* __restrict__ w, const T* __restrict__ bias,
+            T* __restrict__ out) {
+  constexpr int KK = K * K;
+  extern __shared__ __align__(16) float psm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b0 = warp * 2 * g.BS;
+  zero_buffers(psm, b0, g.BS, lane);  // the halo (and an absent bias) stays zero
+  const int pl = lane / g.L, ox = lane - pl * g.L;
+  const RowCopier rc(g, lane);
+  const int N = (int)c.N;
+  const int items = (int)c.C * g.gpc;
+  // consecutive samples of one channel are this far apart in `in`
+  const int64_t pstride = MODE == 0 ? c.x_base(1, 0) : c.y_base(1, 0) - c.y_base(0, 0);
+  const uint32_t nw = gridDim.x * kWarps, wi = blockIdx.x * kWarps + warp;
+  const int ia = (int)((uint64_t)items * wi / nw), ib = (int)((uint64_t)items * (wi + 1) / nw);
+  auto in_base = [&](int n, int ch) -> int64_t { return MODE == 0 ? c.x_base(n, ch) : c.y_base(n, ch); };
+  auto out_base = [&](int n, int ch) -> int64_t { return MODE == 0 ? c.y_base(n, ch) : c.x_base(n, ch); };
+  Cursor ci{g.gpc > 0 ? ia / g.gpc : 0, g.gpc > 0 ? ia % g.gpc : 0}, cc = ci;
+  auto issue = [&](int buf) {
+    const int n0 = ci.j * g.P;
+    rc.run<T>(psm, buf, in + in_base(n0, ci.ch), pstride, min(g.P, N - n0), g);
+    if (lane < KK) {
+      if (sizeof(T) == 4) cp4((uint32_t)__cvta_generic_to_shared(psm + buf + g.XO + lane), w + ci.ch * KK + lane);
+      else psm[buf + g.XO + lane] = ld(w + ci.ch * KK + lane);
+    } else if (lane == KK && MODE == 0 && bias != nullptr) {
+      if (sizeof(T) == 4) cp4((uint32_t)__cvta_generic_to_shared(psm + buf + g.XO + KK), bias + ci.ch);
+      else psm[buf + g.XO + KK] = ld(bias + ci.ch);
+    }
+    ci.next(g.gpc);
+  };
+  auto compute = [&](int buf) {
+    const int ch = cc.ch, n = cc.j * g.P + pl;
+    cc.next(g.gpc);
+    if (ox >= g.Wout || n >= N) return;
+    const float* const wt = psm + buf + g.XO;
+    float wr[KK];
+#pragma unroll
+    for (int i = 0; i < KK; ++i) wr[i] = wt[MODE == 1 ? KK - 1 - i : i];
+    const float bv = wt[KK];
+    T* op = out + out_base(n, ch) + ox;
+    const int wo = g.Wout;
+    walk_rows<K, S, HB>(psm, buf + pl * g.TS + (kCO - g.pad) + ox * S, g.TP, g.Hout, [&](float (&win)[K][K]) {
       float acc = bv;
 #pragma unroll
       for (int a = 0; a < K; ++a)
 #pragma unroll
         for (int b = 0; b < K; ++b) acc = fmaf(wr[a * K + b], win[a][b], acc);
-      T* o = dst + oy * g.Wout + ox;
-      *o = from_f<T>(accumulate ? acc + ld_rw(o) : acc);
-    }
+      *op = from_f<T>(ACC ? acc + ld_rw(op) : acc);
+      op += wo;
+    });
   };
-  warp_walk((int64_t)blockIdx.x * kWarps + warp, (int64_t)gridDim.x * kWarps, g.groups, buf0, buf1, issue,
-            compute);
+  warp_run(ia, ib, b0, b0 + g.BS, issue, compute);
 }
 
-// Weight-gradient first pass: for unit (chunk, channel c),
-// partial[chunk, c, a*K + b] = sum over the chunk's samples of sum_{oy,ox} gy*x̃,
-// partial[chunk, c, K*K] = sum of gy. Warp w takes sample groups w, w + 8, ...
-// of the chunk (P samples per group, one per lane group); lanes keep K*K + 1
-// sums, reduced at the end by a butterfly and then over warps in order.
-template <typename T, int K, int S>
-__global__ void __launch_bounds__(kThreads)
+// Weight-gradient first pass: for unit (chunk cq, channel c),
+// partial[cq, c, a*K + b] = sum over the chunk's samples of sum_{oy,ox} gy*x̃,
+// partial[cq, c, K*K] = sum of gy. Units are ordered channel-major
+// (u = c*chunks + cq); global warp w owns units [U*w/Wt, U*(w+1)/Wt) and
+// walks their G sample groups each (P samples per group, one per lane group)
+// as one run of work items. A tile buffer holds the group's P zero-haloed x
+// plane slots and then its P grad_out planes (GS floats apart). Each lane
+// keeps K*K + 1 sums; at the end of a unit a butterfly adds them over the
+// warp in a fixed order and lanes 0..K*K write the unit's partial. HB > 0:
+// every output plane has HB rows.
+template <typename T, int K, int S, int HB>
+__global__ void __launch_bounds__(kThreads, 3)
 wgrad_kernel(Conv c, PCfg g, const T* __restrict__ x, const T* __restrict__ gy, float* __restrict__ ws,
              int chunks) {
   extern __shared__ __align__(16) float psm[];
   constexpr int NV = K * K + 1;
-  __shared__ float red[kWarps][NV];
+  const int nwarps = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* const buf0 = psm + warp * 2 * g.P * g.TS;
-  float* const buf1 = buf0 + g.P * g.TS;
-  for (int i = lane; i < 2 * g.P * g.TS; i += 32) buf0[i] = 0.f;
-  __syncwarp();
+  const int b0 = warp * 2 * g.BS;
+  zero_buffers(psm, b0, g.BS, lane);
   const int pl = lane / g.L, ox = lane - pl * g.L;
-  int lr, lc, rstep;
-  load_rows_setup(g, lane, lr, lc, rstep);
-  const int64_t units = c.C * chunks;
-  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
-    uint32_t cq;
-    const int64_t ch = c.dC.divmod((uint32_t)u, cq);
-    const int64_t n0 = (int64_t)cq * g.nb;
-    int64_t n1 = n0 + g.nb;
-    if (n1 > c.N) n1 = c.N;
-    float acc[NV];
-#pragma unroll
-    for (int i = 0; i < NV; ++i) acc[i] = 0.f;
-    auto issue = [&](int64_t s0, float* tile) {
-      for (int q = 0; q < g.P; ++q) {
-        if (s0 + q >= n1) break;
-        load_plane<T>(tile + q * g.TS, x + c.x_base(s0 + q, ch), g, g.pad, lr, lc, rstep);
+  const RowCopier rc(g, lane);
+  // (N * C < 2^31, so units, items and samples all fit 32 bits)
+  const int N = (int)c.N, G = g.G;
+  const int units = (int)c.C * chunks;
+  const uint32_t nw = gridDim.x * nwarps, wi = blockIdx.x * nwarps + warp;
+  const int ua = (int)((uint64_t)units * wi / nw), ub = (int)((uint64_t)units * (wi + 1) / nw);
+  const int64_t xstride = c.x_base(1, 0), gstride = c.y_base(1, 0) - c.y_base(0, 0);
+  // grad_out planes are copied as chunks of ggran floats, flattened over the
+  // group's planes: lane's chunks lane, lane + 32, ... as (plane, chunk)
+  const int ghw = g.Hout * g.Wout, cpp = ghw / g.ggran;
+  const int gq0 = lane / cpp, gc0 = lane - gq0 * cpp, gdq = 32 / cpp, gdc = 32 - gdq * cpp;
+  // unit cursor: channel ch, chunk cq, sample group k (samples
+  // [cq*nb + k*P, min(cq*nb + k*P + P, chunk end)))
+  struct UCur {
+    int ch, cq, k;
+  };
+  auto next = [&](UCur& u) {
+    if (++u.k == G) {
+      u.k = 0;
+      if (++u.cq == chunks) {
+        u.cq = 0;
+        ++u.ch;
       }
-    };
-    auto compute = [&](int64_t s0, const float* tile) {
-      const int64_t n = s0 + pl;
-      if (ox >= g.Wout || n >= n1) return;
-      const T* gp = gy + c.y_base(n, ch) + ox;
-      const float* tp = tile + pl * g.TS + ox * S;
-      float win[K][K];
+    }
+  };
+  float acc[NV];
 #pragma unroll
-      for (int a = 0; a < K - S; ++a)
-#pragma unroll
-        for (int b = 0; b < K; ++b) win[a + S][b] = tp[a * g.TP + b];
-      for (int oy = 0; oy < g.Hout; ++oy) {
-#pragma unroll
-        for (int a = 0; a < K - S; ++a)
-#pragma unroll
-          for (int b = 0; b < K; ++b) win[a][b] = win[a + S][b];
-        const float* rowp = tp + oy * S * g.TP;
-#pragma unroll
-        for (int a = K - S; a < K; ++a)
-#pragma unroll
-          for (int b = 0; b < K; ++b) win[a][b] = rowp[a * g.TP + b];
-        const float gv = ld(gp + oy * g.Wout);
+  for (int i = 0; i < NV; ++i) acc[i] = 0.f;
+  UCur ci{ua / chunks, ua % chunks, 0}, cc = ci;
+  auto issue = [&](int buf) {
+    const int c0 = ci.cq * g.nb, s0 = c0 + ci.k * g.P, np = min(g.P, min(c0 + g.nb, N) - s0);
+    if (np > 0) {
+      rc.run<T>(psm, buf, x + c.x_base(s0, ci.ch), xstride, np, g);
+      const T* gp0 = gy + c.y_base(s0, ci.ch);
+      const uint32_t sb = (uint32_t)__cvta_generic_to_shared(psm);
+      for (int q = gq0, cc4 = gc0; q < np;) {
+        const int di = buf + g.XO + q * g.GS + cc4 * g.ggran;
+        const T* sp = gp0 + q * gstride + cc4 * g.ggran;
+        if (sizeof(T) != 4) psm[di] = ld(sp);
+        else if (g.ggran == 4) cp16(sb + 4u * di, sp);
+        else cp4(sb + 4u * di, sp);
+        cc4 += gdc;
+        q += gdq;
+        if (cc4 >= cpp) {
+          cc4 -= cpp;
+          ++q;
+        }
+      }
+    }
+    next(ci);
+  };
+  auto compute = [&](int buf) {
+    const int ch = cc.ch, cq = cc.cq, k = cc.k;
+    next(cc);
+    const int c0 = cq * g.nb, s0 = c0 + k * g.P, s1 = min(c0 + g.nb, N);
+    // an item with fewer than P samples (end of the last chunk) leaves some
+    // lane groups idle; items past that end are empty. A unit flushes once,
+    // at the item holding its last sample (item 0 when the batch is empty:
+    // the partial is then zero).
+    const bool last = k == (cq == chunks - 1 ? g.klast : G - 1);
+    if (ox < g.Wout && s0 + pl < s1) {
+      int gi = buf + g.XO + pl * g.GS + ox;
+      const int wo = g.Wout;
+      walk_rows<K, S, HB>(psm, buf + pl * g.TS + (kCO - g.pad) + ox * S, g.TP, g.Hout, [&](float (&win)[K][K]) {
+        const float gv = psm[gi];
+        gi += wo;
 #pragma unroll
         for (int a = 0; a < K; ++a)
 #pragma unroll
           for (int b = 0; b < K; ++b) acc[a * K + b] = fmaf(gv, win[a][b], acc[a * K + b]);
         acc[K * K] += gv;
+      });
+    }
+    if (last) {
+      float mine = 0.f;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        float v = acc[i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == i) mine = v;
+        acc[i] = 0.f;
       }
-    };
-    warp_walk(n0 + (int64_t)warp * g.P, (int64_t)kWarps * g.P, n1, buf0, buf1, issue, compute);
-    // butterfly within the warp, then the warps in order
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      float v = acc[i];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0) red[warp][i] = v;
+      if (lane < NV) ws[((int64_t)cq * c.OC() + ch) * NV + lane] = mine;
     }
-    __syncthreads();
-    if (threadIdx.x < NV) {
-      float sum = 0.f;
-#pragma unroll
-      for (int wi = 0; wi < kWarps; ++wi) sum += red[wi][threadIdx.x];
-      ws[((int64_t)cq * c.OC() + ch) * NV + threadIdx.x] = sum;
-    }
-    __syncthreads();
-  }
+  };
+  warp_run(ua * G, ub * G, b0, b0 + g.BS, issue, compute);
 }
 
 // Shapes served here: 3x3, stride 1 or 2, dilation 1, one filter per channel,
@@ -262,72 +404,129 @@ bool shape_ok(const Conv& c) {
   return true;
 }
 
-size_t smem_of(const PCfg& g) { return (size_t)kWarps * 2 * g.P * g.TS * sizeof(float); }
+size_t smem_of(const PCfg& g, int warps) { return (size_t)warps * 2 * g.BS * sizeof(float); }
 
-int grid_of(const void* kern, size_t smem, int64_t work) {
-  int dev = 0, sms = 152, per = 1;
+int resident(const void* kern, int threads, size_t smem) {
+  int per = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kern, threads, smem) != cudaSuccess || per < 1) per = 1;
+  return per;
+}
+
+int grid_of(const void* kern, int threads, size_t smem, int64_t work) {
+  int dev = 0, sms = 152;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kern, kThreads, smem) != cudaSuccess || per < 1) per = 1;
-  const int64_t cap = (int64_t)sms * per;
+  const int64_t cap = (int64_t)sms * resident(kern, threads, smem);
   return (int)(work < cap ? (work > 0 ? work : 1) : cap);
 }
 
-// Correlation geometry for MODE 0 / 1.
-PCfg conv_cfg(const Conv& c, bool grad) {
+// Correlation geometry for MODE 0 / 1 (and the weight gradient's x planes);
+// src is the first plane read, for the 8-byte copy alignment test.
+PCfg conv_cfg(const Conv& c, bool grad, const void* src) {
   PCfg g{};
   g.Hin = grad ? (int)c.Ho : (int)c.H;
   g.Win = grad ? (int)c.Wo : (int)c.W;
   g.Hout = grad ? (int)c.H : (int)c.Ho;
   g.Wout = grad ? (int)c.W : (int)c.Wo;
   g.pad = grad ? c.kh - 1 - c.ph : c.ph;
-  const int S = grad ? 1 : c.sh;
+  const int S = grad ? 1 : c.sh, K = c.kh;
   g.L = pow2_at_least(g.Wout);
   g.P = 32 / g.L;
-  g.Lw = pow2_at_least(g.Win);
-  g.TR = (g.Hout - 1) * S + c.kh;
-  g.TP = (g.Wout - 1) * S + c.kw;
+  // 8-byte copies when every plane row starts 8-byte aligned
+  const int64_t hw_in = (int64_t)g.Hin * g.Win;
+  g.gran = (c.dtype == DWCONV_F32 && g.Win % 2 == 0 && hw_in % 2 == 0 && ((uintptr_t)src & 7) == 0) ? 2 : 1;
+  g.Lw = pow2_at_least(g.gran == 2 ? g.Win / 2 : g.Win);
+  g.TR = (g.Hout - 1) * S + K;
+  g.TP = std::max(kCO + g.Win, kCO - g.pad + (g.Wout - 1) * S + K);
+  g.TP += g.TP & 1;
   g.TS = g.TR * g.TP;
-  g.nplanes = c.N * c.C;
-  g.groups = (g.nplanes + g.P - 1) / g.P;
+  // stride 1: the P planes' lanes read P disjoint bank ranges
+  if (S == 1 && g.L >= 2) g.TS = round_to_residue(g.TS, g.L);
+  g.XO = (g.P * g.TS + 3) / 4 * 4;
+  g.GS = g.L >= 2 ? round_to_residue(g.Hout * g.Wout, g.L) : g.Hout * g.Wout;
+  g.BS = (g.XO + K * K + 1 + 3) / 4 * 4;
+  g.gpc = (int)((c.N + g.P - 1) / g.P);
   return g;
+}
+
+// Plane heights with fully unrolled row walks (the fp32 MobileNet planes:
+// 14 and 7 rows, and 4 for the 7x7 stride-2 weight gradient); 0 = any height.
+template <typename T, typename F>
+cudaError_t with_height(int h, F f) {
+  if (sizeof(T) == 4) {
+    if (h == 14) return f(std::integral_constant<int, 14>());
+    if (h == 7) return f(std::integral_constant<int, 7>());
+    if (h == 4) return f(std::integral_constant<int, 4>());
+  }
+  return f(std::integral_constant<int, 0>());
+}
+
+template <typename T, int S, int HB>
+cudaError_t fwd_h(const Conv& c, const PCfg& g, const void* x, const void* w, const void* b, void* y,
+                  cudaStream_t s) {
+  auto kern = conv_kernel<T, 3, S, 0, false, HB>;
+  const size_t smem = smem_of(g, kWarps);
+  cudaError_t e = tile::set_smem(kern, smem);
+  if (e != cudaSuccess) return e;
+  const int grid = grid_of((const void*)kern, kThreads, smem, (c.C * g.gpc + kWarps - 1) / kWarps);
+  kern<<<grid, kThreads, smem, s>>>(c, g, (const T*)x, (const T*)w, (const T*)b, (T*)y);
+  return cudaGetLastError();
 }
 
 template <typename T, int S>
 cudaError_t fwd_t(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s) {
-  const PCfg g = conv_cfg(c, false);
-  auto kern = conv_kernel<T, 3, S, 0>;
-  const size_t smem = smem_of(g);
+  const PCfg g = conv_cfg(c, false, x);
+  return with_height<T>(g.Hout, [&](auto hb) { return fwd_h<T, S, decltype(hb)::value>(c, g, x, w, b, y, s); });
+}
+
+template <typename T, bool ACC, int HB>
+cudaError_t bwd1_h(const Conv& c, const PCfg& g, const void* gy, const void* w, void* gx, cudaStream_t s) {
+  auto kern = conv_kernel<T, 3, 1, 1, ACC, HB>;
+  const size_t smem = smem_of(g, kWarps);
   cudaError_t e = tile::set_smem(kern, smem);
   if (e != cudaSuccess) return e;
-  const int grid = grid_of((const void*)kern, smem, (g.groups + kWarps - 1) / kWarps);
-  kern<<<grid, kThreads, smem, s>>>(c, g, (const T*)x, (const T*)w, (const T*)b, (T*)y, 0);
+  const int grid = grid_of((const void*)kern, kThreads, smem, (c.C * g.gpc + kWarps - 1) / kWarps);
+  kern<<<grid, kThreads, smem, s>>>(c, g, (const T*)gy, (const T*)w, nullptr, (T*)gx);
   return cudaGetLastError();
 }
 
-template <typename T>
-cudaError_t bwd1_t(const Conv& c, const void* gy, const void* w, void* gx, bool acc, cudaStream_t s) {
-  const PCfg g = conv_cfg(c, true);
-  auto kern = conv_kernel<T, 3, 1, 1>;
-  const size_t smem = smem_of(g);
-  cudaError_t e = tile::set_smem(kern, smem);
-  if (e != cudaSuccess) return e;
-  const int grid = grid_of((const void*)kern, smem, (g.groups + kWarps - 1) / kWarps);
-  kern<<<grid, kThreads, smem, s>>>(c, g, (const T*)gy, (const T*)w, nullptr, (T*)gx, acc ? 1 : 0);
+template <typename T, bool ACC>
+cudaError_t bwd1_t(const Conv& c, const void* gy, const void* w, void* gx, cudaStream_t s) {
+  const T* first = (const T*)gy + c.y_base(0, 0);
+  const PCfg g = conv_cfg(c, true, first);
+  return with_height<T>(g.Hout, [&](auto hb) { return bwd1_h<T, ACC, decltype(hb)::value>(c, g, gy, w, gx, s); });
+}
+
+template <typename T, int S, int HB>
+cudaError_t wgrad_h(const Conv& c, const PCfg& g, const void* x, const void* gy, float* ws, int chunks,
+                    cudaStream_t s) {
+  auto kern = wgrad_kernel<T, 3, S, HB>;
+  // warps are independent: take the CTA size (8 or 4 warps) that keeps more
+  // warps resident under the tile buffers' shared memory
+  int warps = kWarps;
+  {
+    const size_t s8 = smem_of(g, 8), s4 = smem_of(g, 4);
+    cudaError_t e = tile::set_smem(kern, s8 > s4 ? s8 : s4);
+    if (e != cudaSuccess) return e;
+    if (4 * resident((const void*)kern, 128, s4) > 8 * resident((const void*)kern, 256, s8)) warps = 4;
+  }
+  const size_t smem = smem_of(g, warps);
+  const int64_t units = c.C * chunks;
+  const int grid = grid_of((const void*)kern, warps * 32, smem, (units + warps - 1) / warps);
+  kern<<<grid, warps * 32, smem, s>>>(c, g, (const T*)x, (const T*)gy, ws, chunks);
   return cudaGetLastError();
 }
 
 template <typename T, int S>
 cudaError_t wgrad_t(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s) {
-  PCfg g = conv_cfg(c, false);
+  PCfg g = conv_cfg(c, false, x);
+  g.BS = (g.XO + g.P * g.GS + 3) / 4 * 4;
+  g.ggran = (c.dtype == DWCONV_F32 && (g.Hout * g.Wout) % 4 == 0 && g.GS % 4 == 0 && ((uintptr_t)gy & 15) == 0)
+                ? 4 : 1;
   g.nb = (int)wgrad_nb(c);
+  g.G = (g.nb + g.P - 1) / g.P;
+  g.klast = c.N > 0 ? (int)((c.N - (int64_t)(chunks - 1) * g.nb - 1) / g.P) : 0;
   if (c.N > 0 && (c.N + g.nb - 1) / g.nb != chunks) return cudaErrorInvalidConfiguration;
-  auto kern = wgrad_kernel<T, 3, S>;
-  const size_t smem = smem_of(g);
-  cudaError_t e = tile::set_smem(kern, smem);
-  if (e != cudaSuccess) return e;
-  const int grid = grid_of((const void*)kern, smem, c.C * chunks);
-  kern<<<grid, kThreads, smem, s>>>(c, g, (const T*)x, (const T*)gy, ws, chunks);
-  return cudaGetLastError();
+  return with_height<T>(g.Hout, [&](auto hb) { return wgrad_h<T, S, decltype(hb)::value>(c, g, x, gy, ws, chunks, s); });
 }
 
 }  // namespace
@@ -337,14 +536,26 @@ bool bwd_data_supported(const Conv& c) { return shape_ok(c) && c.sh == 1 && c.W 
 bool wgrad_supported(const Conv& c) { return shape_ok(c) && c.Wo <= 16; }
 
 int64_t wgrad_nb(const Conv& c) {
-  // a chunk is a whole number of sample groups for every warp of a CTA
-  // (P samples per warp group), with at least about four units per SM
-  const int P = 32 / pow2_at_least((int)c.Wo);
-  int64_t nb = (int64_t)P * kWarps;
-  const int64_t units_min = 152 * 4;
-  while (nb > P && c.C * ((c.N + nb - 1) / nb) < units_min) nb -= P;
-  if (nb > c.N) nb = c.N > 0 ? c.N : 1;
-  return nb;
+  // A warp owns whole (chunk, channel) units of G sample groups (P samples
+  // each): take the G whose busiest warp -- ceil(units / warps) units, each
+  // G groups plus one warp reduction (about a third of a group) -- is
+  // shortest, for about 3 x 8 resident warps per SM on 152 SMs.
+  const int64_t P = 32 / pow2_at_least((int)c.Wo);
+  const int64_t warps = 152 * 24;
+  int64_t best = P;
+  double best_cost = 0.0;
+  for (int64_t G = 1; G <= 8; ++G) {
+    const int64_t nb = G * P;
+    const int64_t units = c.C * ((c.N + nb - 1) / nb);
+    const double cost = (double)((units + warps - 1) / warps) * ((double)G + 0.35);
+    if (G == 1 || cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = nb;
+    }
+    if (nb >= c.N) break;
+  }
+  if (best > c.N) best = c.N > 0 ? c.N : 1;
+  return best;
 }
 
 int wgrad_chunks(const Conv& c) {
@@ -365,7 +576,11 @@ cudaError_t fwd(const Conv& c, const void* x, const void* w, const void* b, void
 cudaError_t bwd_data(const Conv& c, const void* gy, const void* w, void* gx, bool acc, cudaStream_t s) {
   cudaError_t e = cudaErrorInvalidConfiguration;
   if (c.sh != 1) return e;
-  DWCONV_DISPATCH_DTYPE(c.dtype, T, e = bwd1_t<T>(c, gy, w, gx, acc, s));
+  if (acc) {
+    DWCONV_DISPATCH_DTYPE(c.dtype, T, e = (bwd1_t<T, true>(c, gy, w, gx, s)));
+  } else {
+    DWCONV_DISPATCH_DTYPE(c.dtype, T, e = (bwd1_t<T, false>(c, gy, w, gx, s)));
+  }
   return e;
 }
 

@@ -432,6 +432,20 @@ def test_plane_kernels_vs_oracle(L):
     check_full(L, WL.make_inputs(L), L.label())
 
 
+def test_plane_wgrad_unit_with_empty_group():
+    """62 samples, 128 channels of 14x14: the weight gradient's units are two
+    sample groups of two samples (16 chunks of 4 samples, so 16 * 128 * 10
+    fp32 partials); the last chunk holds samples 60, 61 only, so its second
+    group is empty and must not overwrite the unit's partial."""
+    L = WL.Layer(N=62, C=128, H=14, W=14, k=3, s=1, p=1, bias=True, dtype="f32")
+    d = desc_of(L)
+    assert B.dwconv2d_plan_name(d, 2) == "plane"
+    _, nbytes = ws_for(d)
+    assert nbytes >= 16 * L.OC * 10 * 4
+    assert nbytes < 17 * L.OC * 10 * 4
+    check_full(L, WL.make_inputs(L), L.label())
+
+
 @pytest.mark.parametrize("L", [PLANE_CASES[0], PLANE_CASES[1]], ids=PLANE_IDS[:2])
 def test_plane_slices_and_accumulate(L):
     """Output slice written in place, grad_out read from the slice, grad-input accumulates."""
