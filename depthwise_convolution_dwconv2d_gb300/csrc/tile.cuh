@@ -50,6 +50,15 @@ __device__ __forceinline__ void cp_async4(void* smem, const void* gmem, int src_
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(s), "l"(gmem), "r"(src_bytes)
                : "memory");
 }
+// One entry of a stage's side table (filter taps, bias): fp32 by an
+// asynchronous 4-byte copy that completes with the stage's cp.async group
+// (so no thread waits on a global load while the previous stage computes),
+// 16-bit types widened through a register.
+template <typename T>
+__device__ __forceinline__ void tab_put(float* dst, const T* src) {
+  if (sizeof(T) == 4) cp_async4(dst, src, 4);
+  else *dst = ld(src);
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {

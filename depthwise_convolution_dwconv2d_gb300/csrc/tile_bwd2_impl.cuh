@@ -99,7 +99,7 @@ bwd2_kernel(Conv c, Bwd2Cfg g, const __grid_constant__ CUtensorMap tmap, unsigne
       c.split(p0 + pl, n, ch);
       const T* wp = w + (ch * m + (sj - pl * m)) * (K * K);
 #pragma unroll
-      for (int i = 0; i < K * K; ++i) tab[sj * (K * K) + i] = ld(wp + i);
+      for (int i = 0; i < K * K; ++i) tab_put(tab + sj * (K * K) + i, wp + i);
     }
     if (g.mode == kCopyDense) {
       if (g.contig)

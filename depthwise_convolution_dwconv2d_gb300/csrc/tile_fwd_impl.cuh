@@ -78,8 +78,9 @@ fwd_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned int
       const int64_t oc = ch * c.m + (pj - pl * c.m);
       const T* wp = w + oc * (K * K);
 #pragma unroll
-      for (int tap = 0; tap < K * K; ++tap) wt[pj * (K * K) + tap] = ld(wp + tap);
-      bt[pj] = bias ? ld(bias + oc) : 0.f;
+      for (int tap = 0; tap < K * K; ++tap) tab_put(wt + pj * (K * K) + tap, wp + tap);
+      if (bias) tab_put(bt + pj, bias + oc);
+      else bt[pj] = 0.f;
       ot[pj] = c.y_base(n, oc);
     }
   };
@@ -208,7 +209,7 @@ bwd1_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned in
       c.split(p0 + pl, n, ch);
       const T* wp = w + (ch * m + (s - pl * m)) * (K * K);
 #pragma unroll
-      for (int tap = 0; tap < K * K; ++tap) tab[s * (K * K) + tap] = ld(wp + (K * K - 1 - tap));
+      for (int tap = 0; tap < K * K; ++tap) tab_put(tab + s * (K * K) + tap, wp + (K * K - 1 - tap));
     }
     for (int pl = threadIdx.x; pl < np; pl += kNT) ot[pl] = (p0 + pl) * c.H * c.W;
   };
