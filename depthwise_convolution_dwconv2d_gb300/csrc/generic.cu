@@ -132,20 +132,31 @@ bwd_weight_generic_pass1_kernel(Conv c, const T* __restrict__ x, const T* __rest
   }
 }
 
+// One warp per output: the lanes load chunks lane, lane + 32, ... at once
+// (one memory round trip per 32 chunks instead of one per chunk), then every
+// lane runs the same sum over the shuffled values in chunk index order, so
+// the rounding is that of the plain sequential sum.
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 bwd_weight_pass2_kernel(Conv c, const float* __restrict__ ws, int chunks, T* gw, T* gb) {
   const int taps = c.kh * c.kw;
   const int64_t total = c.OC() * (taps + 1);
-  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
-       idx += (int64_t)gridDim.x * blockDim.x) {
+  const int lane = threadIdx.x & 31;
+  const int64_t wpb = blockDim.x >> 5;
+  for (int64_t idx = blockIdx.x * wpb + (threadIdx.x >> 5); idx < total; idx += (int64_t)gridDim.x * wpb) {
     const int64_t oc = idx / (taps + 1);
     const int tap = (int)(idx % (taps + 1));
-    if (tap < taps ? gw == nullptr : gb == nullptr) continue;
+    if (tap < taps ? gw == nullptr : gb == nullptr) continue;  // warp-uniform
     float s = 0.f;
-    for (int k = 0; k < chunks; ++k) s += ws[(int64_t)k * total + idx];
-    if (tap < taps) gw[oc * taps + tap] = from_f<T>(s);
-    else gb[oc] = from_f<T>(s);
+    for (int kb = 0; kb < chunks; kb += 32) {
+      const float v = kb + lane < chunks ? ws[(int64_t)(kb + lane) * total + idx] : 0.f;
+      const int nk = chunks - kb < 32 ? chunks - kb : 32;
+      for (int j = 0; j < nk; ++j) s += __shfl_sync(0xffffffffu, v, j);
+    }
+    if (lane == 0) {
+      if (tap < taps) gw[oc * taps + tap] = from_f<T>(s);
+      else gb[oc] = from_f<T>(s);
+    }
   }
 }
 
@@ -234,7 +245,7 @@ cudaError_t bwd_weight_generic_pass1(const Conv& c, const void* x, const void* g
 
 cudaError_t bwd_weight_pass2(const Conv& c, const float* ws, int chunks, void* gw, void* gb,
                              cudaStream_t s) {
-  const int g = grid_for(c.OC() * (c.kh * c.kw + 1));
+  const int g = grid_for(c.OC() * (c.kh * c.kw + 1) * 32);  // a warp per output
   DWCONV_DISPATCH_DTYPE(c.dtype, T,
     bwd_weight_pass2_kernel<T><<<g, kThreads, 0, s>>>(c, ws, chunks, (T*)gw, (T*)gb));
   return cudaGetLastError();
