@@ -240,9 +240,12 @@ bwd2_kernel(Conv c, Bwd2Cfg g, const __grid_constant__ CUtensorMap tmap, unsigne
           for (int v = 0; v < V; ++v)
 #pragma unroll
             for (int pw = 0; pw < S; ++pw) o[v * S + pw] = acc[r][ph][v][pw];
-          if (g.vec_out && (S * V) % 4 == 0 && col0 + S * V <= c.W) {
+          if (g.vec_out && (S * V) % 4 == 0) {
+            // W % 4 == 0 and col0 % 4 == 0: every group of four columns is
+            // wholly inside the row or wholly past its end
 #pragma unroll
             for (int q = 0; q < S * V / 4; ++q) {
+              if (col0 + 4 * q >= c.W) break;
               float f[4];
 #pragma unroll
               for (int i = 0; i < 4; ++i)
