@@ -91,7 +91,8 @@ __device__ __forceinline__ void cp16(uint32_t s, const void* g) {
 // rest of a slot (the zero halo) is never written. The warp walks the
 // group's rows flattened over the planes: lane (lr, lc) copies granule lc of
 // rows lr, lr + rstep, ..., advancing its (plane, row) cursor by a constant
-// step (no per-plane setup, no division). fp32 goes by asynchronous copies
+// step (no per-plane setup, no division); tall planes (about 16 rows or
+// more) are walked one by one instead. fp32 goes by asynchronous copies
 // (completed by the caller's wait), 16-bit types are widened through
 // registers.
 struct RowCopier {
@@ -107,18 +108,35 @@ struct RowCopier {
     dq = rstep / g.Hin;
     dr = rstep - dq * g.Hin;
   }
-  template <typename T>
+  // TALL: 1 = per-plane loops, 0 = flattened walk, -1 = choose by the plane
+  // height at run time
+  template <int TALL, typename T>
   __device__ __forceinline__ void run(float* psm, int slot0, const T* __restrict__ src0, int64_t pstride, int np,
                                       const PCfg& g) const {
     const int cw = (sizeof(T) == 4 ? g.gran : 1) * lc;
     if (cw >= g.Win) return;
     const int rend = min(g.Hin, g.TR - g.pad);
+    const uint32_t sb = (uint32_t)__cvta_generic_to_shared(psm);
+    if (TALL == 1 || (TALL < 0 && g.Hin >= 16)) {
+      // tall planes: a plain unrolled row loop per plane (its setup is paid
+      // over many rows)
+      for (int q = 0; q < np; ++q) {
+        int di = slot0 + q * g.TS + (g.pad + lr) * g.TP + kCO + cw;
+        const T* sp = src0 + q * pstride + lr * g.Win + cw;
+#pragma unroll 4
+        for (int r = lr; r < rend; r += rstep, di += rstep * g.TP, sp += rstep * g.Win) {
+          if (sizeof(T) != 4) psm[di] = ld(sp);
+          else if (g.gran == 2) cp8(sb + 4u * di, sp);
+          else cp4(sb + 4u * di, sp);
+        }
+      }
+      return;
+    }
     int q = q0, r = r0;
     int di = slot0 + q * g.TS + (r + g.pad) * g.TP + kCO + cw;
     const T* sp = src0 + q * pstride + r * g.Win + cw;
     const int dstep = dq * g.TS + dr * g.TP, dwrap = g.TS - g.Hin * g.TP;
     const int64_t sstep = dq * pstride + dr * g.Win, swrap = pstride - (int64_t)g.Hin * g.Win;
-    const uint32_t sb = (uint32_t)__cvta_generic_to_shared(psm);
     while (q < np) {
       if (r < rend) {
         if (sizeof(T) != 4) psm[di] = ld(sp);
@@ -250,7 +268,7 @@ conv_kernel(Conv c, PCfg g, const T* __restrict__ in, const T* __restrict__ w, c
   Cursor ci{g.gpc > 0 ? ia / g.gpc : 0, g.gpc > 0 ? ia % g.gpc : 0}, cc = ci;
   auto issue = [&](int buf) {
     const int n0 = ci.j * g.P;
-    rc.run<T>(psm, buf, in + in_base(n0, ci.ch), pstride, min(g.P, N - n0), g);
+    rc.run<HB == 0 ? -1 : (HB * S >= 16 ? 1 : 0)>(psm, buf, in + in_base(n0, ci.ch), pstride, min(g.P, N - n0), g);
     if (lane < KK) {
       if (sizeof(T) == 4) cp4((uint32_t)__cvta_generic_to_shared(psm + buf + g.XO + lane), w + ci.ch * KK + lane);
       else psm[buf + g.XO + lane] = ld(w + ci.ch * KK + lane);
@@ -337,7 +355,7 @@ wgrad_kernel(Conv c, PCfg g, const T* __restrict__ x, const T* __restrict__ gy, 
   auto issue = [&](int buf) {
     const int c0 = ci.cq * g.nb, s0 = c0 + ci.k * g.P, np = min(g.P, min(c0 + g.nb, N) - s0);
     if (np > 0) {
-      rc.run<T>(psm, buf, x + c.x_base(s0, ci.ch), xstride, np, g);
+      rc.run<HB == 0 ? -1 : (HB * S >= 16 ? 1 : 0)>(psm, buf, x + c.x_base(s0, ci.ch), xstride, np, g);
       const T* gp0 = gy + c.y_base(s0, ci.ch);
       const uint32_t sb = (uint32_t)__cvta_generic_to_shared(psm);
       for (int q = gq0, cc4 = gc0; q < np;) {

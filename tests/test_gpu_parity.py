@@ -414,8 +414,9 @@ PLANE_CASES = [
     WL.Layer(N=2, C=3, H=9, W=16, k=3, s=1, p=0, dtype="f32"),
     WL.Layer(N=2, C=3, H=10, W=11, k=3, s=1, p=2, dtype="f32"),
     WL.Layer(N=17, C=3, H=10, W=11, k=3, s=2, p=2, bias=True, dtype="f32"),
+    WL.Layer(N=3, C=5, H=40, W=12, k=3, s=1, p=1, bias=True, dtype="f32"),
 ]
-PLANE_IDS = ["14s1", "15x13s2", "7s2bf16", "28s2f16", "w16p0", "p2s1", "p2s2N17"]
+PLANE_IDS = ["14s1", "15x13s2", "7s2bf16", "28s2f16", "w16p0", "p2s1", "p2s2N17", "tall40x12"]
 
 
 @pytest.mark.parametrize("L", PLANE_CASES, ids=PLANE_IDS)
