@@ -7,13 +7,14 @@
 // spend most of their instructions on indexing and staging, so here a warp
 // works alone on a few whole planes of one channel (P samples at a time):
 //  * it copies the planes (coalesced rows, 8-byte granules where aligned)
-//    into its own zero-haloed tile in shared memory, together with what the
+//    into its own double-buffered, zero-haloed tile in shared memory (plane
+//    slots offset so that the planes' lanes read disjoint banks), with what the
 //    compute needs next to them (the channel's filter taps and bias; for the
 //    weight gradient the grad_out planes), all with asynchronous copies
 //    issued one work item ahead -- no CTA barrier and no global load on the
 //    compute path;
-//  * each lane owns one output column of one plane (two or four planes per
-//    warp when the planes are narrow) and walks the output rows with the
+//  * each lane owns one output column of one plane (two, four or eight
+//    planes per warp as the rows narrow) and walks the output rows with the
 //    K x K window held in registers (a stride-1 step loads one new row of
 //    K values), so an output costs K shared loads, K*K FMAs and a store;
 //    the walk is unrolled (fully for the common plane heights), with 32-bit
