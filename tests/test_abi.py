@@ -142,3 +142,28 @@ def test_status_strings(lib):
 def test_plan_names(lib):
     assert B.dwconv2d_plan_name(B.make_desc(64, 128, 56, 56, 3, 1, 1), 0) in ("generic", "tile", "large")
     assert B.dwconv2d_plan_name(B.make_desc(64, 128, 56, 56, 3, 1, 1), 3) == "invalid"
+
+
+def test_plane_routing_and_chunking(lib):
+    """Host planning of the small-plane family (no GPU needed): the forward and
+    stride-1 grad-input take it on rows of 9..16, the weight gradient on
+    output rows of at most 16; its weight-gradient chunks cover the batch
+    (1 <= chunks <= N) and size the workspace as chunks x OC x (k*k + 1)
+    fp32 partials."""
+    mk = lambda N, C, H, s: B.make_desc(N, C, H, H, 3, s, 1)
+    assert B.dwconv2d_plan_name(mk(64, 512, 14, 1), 0) == "plane"
+    assert B.dwconv2d_plan_name(mk(64, 512, 14, 1), 1) == "plane"
+    assert B.dwconv2d_plan_name(mk(64, 512, 14, 2), 0) == "plane"
+    assert B.dwconv2d_plan_name(mk(64, 512, 14, 2), 1) == "tile"  # strided grad-input
+    assert B.dwconv2d_plan_name(mk(64, 256, 28, 2), 2) == "plane"  # output rows of 14
+    assert B.dwconv2d_plan_name(mk(64, 256, 28, 1), 2) == "tile"  # output rows of 28
+    assert B.dwconv2d_plan_name(mk(64, 256, 28, 1), 0) == "tile"  # rows of 28
+    for N, C, H, s in [(64, 512, 14, 1), (64, 512, 14, 2), (64, 1024, 7, 2), (64, 256, 28, 2), (62, 128, 14, 1),
+                       (1, 32, 14, 1), (17, 32, 11, 2)]:
+        d = mk(N, C, H, s)
+        assert B.dwconv2d_plan_name(d, 2) == "plane"
+        ws = B.dwconv2d_bwd_weight_workspace_size(d)
+        per_chunk = C * (3 * 3 + 1) * 4  # C a multiple of 32: a whole number of 256-byte blocks
+        assert ws % per_chunk == 0
+        chunks = ws // per_chunk
+        assert 1 <= chunks <= N, (N, C, H, s, chunks)
