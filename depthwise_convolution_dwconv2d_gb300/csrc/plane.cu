@@ -425,6 +425,9 @@ bool shape_ok(const Conv& c) {
 
 size_t smem_of(const PCfg& g, int warps) { return (size_t)warps * 2 * g.BS * sizeof(float); }
 
+// dynamic shared memory a CTA may use (227 KB on this GPU)
+constexpr size_t kSmemMax = 227 * 1024;
+
 int resident(const void* kern, int threads, size_t smem) {
   int per = 1;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kern, threads, smem) != cudaSuccess || per < 1) per = 1;
@@ -521,12 +524,15 @@ cudaError_t wgrad_h(const Conv& c, const PCfg& g, const void* x, const void* gy,
   auto kern = wgrad_kernel<T, 3, S, HB>;
   // warps are independent: take the CTA size (8 or 4 warps) that keeps more
   // warps resident under the tile buffers' shared memory
+  // (4 warps when 8 warps' buffers exceed a CTA's shared memory; the
+  // planner only routes shapes whose 4-warp buffers fit)
   int warps = kWarps;
   {
     const size_t s8 = smem_of(g, 8), s4 = smem_of(g, 4);
-    cudaError_t e = tile::set_smem(kern, s8 > s4 ? s8 : s4);
+    const bool eight = s8 <= kSmemMax;
+    cudaError_t e = tile::set_smem(kern, eight ? s8 : s4);
     if (e != cudaSuccess) return e;
-    if (4 * resident((const void*)kern, 128, s4) > 8 * resident((const void*)kern, 256, s8)) warps = 4;
+    if (!eight || 4 * resident((const void*)kern, 128, s4) > 8 * resident((const void*)kern, 256, s8)) warps = 4;
   }
   const size_t smem = smem_of(g, warps);
   const int64_t units = c.C * chunks;
@@ -535,10 +541,16 @@ cudaError_t wgrad_h(const Conv& c, const PCfg& g, const void* x, const void* gy,
   return cudaGetLastError();
 }
 
-template <typename T, int S>
-cudaError_t wgrad_t(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s) {
+// Weight-gradient geometry: x plane slots, then the P grad_out planes.
+PCfg wgrad_cfg(const Conv& c, const void* x) {
   PCfg g = conv_cfg(c, false, x);
   g.BS = (g.XO + g.P * g.GS + 3) / 4 * 4;
+  return g;
+}
+
+template <typename T, int S>
+cudaError_t wgrad_t(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s) {
+  PCfg g = wgrad_cfg(c, x);
   g.ggran = (c.dtype == DWCONV_F32 && (g.Hout * g.Wout) % 4 == 0 && g.GS % 4 == 0 && ((uintptr_t)gy & 15) == 0)
                 ? 4 : 1;
   g.nb = (int)wgrad_nb(c);
@@ -550,9 +562,18 @@ cudaError_t wgrad_t(const Conv& c, const void* x, const void* gy, float* ws, int
 
 }  // namespace
 
-bool fwd_supported(const Conv& c) { return shape_ok(c) && c.W > 8 && c.W <= 16; }
-bool bwd_data_supported(const Conv& c) { return shape_ok(c) && c.sh == 1 && c.W > 8 && c.W <= 16; }
-bool wgrad_supported(const Conv& c) { return shape_ok(c) && c.Wo <= 16; }
+// A shape is served only when its warps' tile buffers fit a CTA's shared
+// memory (8 warps for the correlation kernels, at least 4 for the weight
+// gradient); taller planes go to the tile kernels.
+bool fwd_supported(const Conv& c) {
+  return shape_ok(c) && c.W > 8 && c.W <= 16 && smem_of(conv_cfg(c, false, nullptr), kWarps) <= kSmemMax;
+}
+bool bwd_data_supported(const Conv& c) {
+  return shape_ok(c) && c.sh == 1 && c.W > 8 && c.W <= 16 && smem_of(conv_cfg(c, true, nullptr), kWarps) <= kSmemMax;
+}
+bool wgrad_supported(const Conv& c) {
+  return shape_ok(c) && c.Wo <= 16 && smem_of(wgrad_cfg(c, nullptr), 4) <= kSmemMax;
+}
 
 int64_t wgrad_nb(const Conv& c) {
   // A warp owns whole (chunk, channel) units of G sample groups (P samples

@@ -158,6 +158,12 @@ def test_plane_routing_and_chunking(lib):
     assert B.dwconv2d_plan_name(mk(64, 256, 28, 2), 2) == "plane"  # output rows of 14
     assert B.dwconv2d_plan_name(mk(64, 256, 28, 1), 2) == "tile"  # output rows of 28
     assert B.dwconv2d_plan_name(mk(64, 256, 28, 1), 0) == "tile"  # rows of 28
+    # tall stride-2 planes: the forward's eight-warp tile buffers would need
+    # about 300 KB of shared memory, so it goes to the tile kernel; the weight
+    # gradient's fit with four warps per CTA
+    tall = B.make_desc(2, 3, 64, 16, 3, 2, 1)
+    assert B.dwconv2d_plan_name(tall, 0) != "plane"
+    assert B.dwconv2d_plan_name(tall, 2) == "plane"
     for N, C, H, s in [(64, 512, 14, 1), (64, 512, 14, 2), (64, 1024, 7, 2), (64, 256, 28, 2), (62, 128, 14, 1),
                        (1, 32, 14, 1), (17, 32, 11, 2)]:
         d = mk(N, C, H, s)

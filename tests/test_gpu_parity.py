@@ -447,6 +447,17 @@ def test_plane_wgrad_unit_with_empty_group():
     check_full(L, WL.make_inputs(L), L.label())
 
 
+def test_plane_tall_strided_planes():
+    """64 x 16 planes at stride 2: the forward's tile buffers do not fit a
+    CTA's shared memory, so it runs on the tile kernel; the weight gradient
+    runs on the plane kernel with four-warp CTAs."""
+    L = WL.Layer(N=2, C=3, H=64, W=16, k=3, s=2, p=1, bias=True, dtype="f32")
+    d = desc_of(L)
+    assert B.dwconv2d_plan_name(d, 0) != "plane"
+    assert B.dwconv2d_plan_name(d, 2) == "plane"
+    check_full(L, WL.make_inputs(L), L.label())
+
+
 @pytest.mark.parametrize("L", [PLANE_CASES[0], PLANE_CASES[1]], ids=PLANE_IDS[:2])
 def test_plane_slices_and_accumulate(L):
     """Output slice written in place, grad_out read from the slice, grad-input accumulates."""
