@@ -14,6 +14,7 @@
 // tile_bwd2_impl.cuh and are compiled once per storage type.
 #include "plan.h"
 #include "tile_cases.h"
+#include "tile_fit.h"
 
 namespace dwconv {
 namespace tile {
@@ -27,6 +28,8 @@ bool bwd2_supported(const Conv& c) {
   if (c.W > 1024 || c.Wo > 1024) return false;
   if (c.ph % c.sh != c.pw % c.sh) return false;
   const int pm = c.ph % c.sh;
+  const int es = c.dtype == DWCONV_F32 ? 4 : 2;
+  if (bwd2_min_bytes(c.kh, c.sh, c.dh, pm, c.W, es, c.m) > 48 * 1024) return false;
 #define X(K, S, D, PM) if (c.kh == K && c.sh == S && c.dh == D && pm == PM) return true;
   DW_BWD2_CASES(X)
 #undef X

@@ -3,6 +3,7 @@
 // per storage type in tile_fwd_{f32,f16,bf16}.cu.
 #include "plan.h"
 #include "tile_cases.h"
+#include "tile_fit.h"
 
 namespace dwconv {
 namespace tile {
@@ -21,6 +22,9 @@ bool square(const Conv& c) {
 bool fwd_supported(const Conv& c) {
   if (!c.planes32()) return false;
   if (!square(c) || c.W > 1024 || c.Wo > 1024) return false;
+  // the planner's narrowest band must fit its 48 KB limit
+  const int es = c.dtype == DWCONV_F32 ? 4 : 2;
+  if (band_min_bytes(c.kh, c.sh, c.dh, c.sh == 1 ? 4 : 2, 4, c.Wo, es, 1) > 48 * 1024) return false;
 #define X(K, S, D) if (c.kh == K && c.sh == S && c.dh == D) return true;
   DW_FWD_CASES(X)
 #undef X
@@ -37,6 +41,8 @@ bool bwd1_supported(const Conv& c) {
   if (!c.planes32()) return false;
   if (!square(c) || c.sh != 1 || c.m > 4 || c.W > 1024 || c.Wo > 1024) return false;
   if (c.ph > c.dh * (c.kh - 1) || c.pw > c.dw * (c.kw - 1)) return false;
+  const int es = c.dtype == DWCONV_F32 ? 4 : 2;
+  if (band_min_bytes(c.kh, 1, c.dh, 4, 4, c.W, es, c.m) > 48 * 1024) return false;
 #define X(K, D) if (c.kh == K && c.dh == D) return true;
   DW_BWD1_CASES(X)
 #undef X

@@ -419,6 +419,46 @@ cudaError_t bwd_multi_t(int nb, const Conv* cs, const void* gy, const void* cons
 
 }  // namespace
 
+// The fused planners' narrowest bands must fit their 96 KB limit: the
+// forward's has L rows (L the lcm of the branches' d*kR), the grad-input's
+// kR rows per branch. Both follow the planners' arithmetic with the widest
+// row pitch any pointer alignment gives (a shift of at most one 16-byte
+// chunk), so a shape that passes always plans.
+bool multi_fits(int nb, const Conv* cs) {
+  const int64_t K = cs[0].kh, es = cs[0].dtype == DWCONV_F32 ? 4 : 2;
+  const int64_t smax = 16 / es - 1, PA = 16 / es > 4 ? 16 / es : 4;
+  auto rup = [](int64_t v, int64_t a) { return (v + a - 1) / a * a; };
+  int64_t hh = 0, hw = 0;
+  int L = 1;
+  for (int b = 0; b < nb; ++b) {
+    hh = cs[b].ph > hh ? cs[b].ph : hh;
+    hw = cs[b].pw > hw ? cs[b].pw : hw;
+    L = lcm(L, cs[b].dh * kR);
+  }
+  int64_t need = 0, tr = 0;
+  for (int b = 0; b < nb; ++b) {
+    const int64_t Q = cs[b].dh, D = cs[b].dh;
+    const int64_t cb = (cs[0].Wo + Q * kV - 1) / (Q * kV);
+    const int64_t WN = (kV - 1) * Q + (K - 1) * D + 1;
+    const int64_t off = hw - cs[b].pw + smax;
+    const int64_t rc = Q == 1 ? (cb - 1) * kV + off + WN + 3 : (cb - 1) * Q * kV + Q - 1 + off + WN;
+    if (rc > need) need = rc;
+    const int64_t r = L - 1 + (hh - cs[b].ph) + (K - 1) * D + 1;
+    if (r > tr) tr = r;
+  }
+  if (tr * rup(need, PA) * es > 96 * 1024) return false;
+  const int64_t cb = (cs[0].W + kV - 1) / kV;
+  int64_t rows = 0;
+  need = 0;
+  for (int b = 0; b < nb; ++b) {
+    const int64_t D = cs[b].dh;
+    const int64_t rc = (cb - 1) * kV + smax + (kV - 1) + (K - 1) * D + 1 + 3;
+    if (rc > need) need = rc;
+    rows += kR - 1 + (K - 1) * D + 1;
+  }
+  return rows * rup(need, PA) * es <= 96 * 1024;
+}
+
 bool multi_supported(int nb, const Conv* cs) {
   if (!same_geometry(nb, cs) || !cs[0].planes32()) return false;
   for (int b = 0; b < nb; ++b) {
@@ -426,6 +466,7 @@ bool multi_supported(int nb, const Conv* cs) {
     // the fused grad-input needs non-negative transposed padding
     if (cs[b].ph > cs[b].dh * (cs[b].kh - 1) || cs[b].pw > cs[b].dw * (cs[b].kw - 1)) return false;
   }
+  if (!multi_fits(nb, cs)) return false;
 #define X(K, NB, D0, D1, D2) \
   if (nb == NB && cs[0].kh == K && cs[0].dh == D0 && cs[1].dh == D1 && (NB < 3 || cs[2].dh == D2)) return true;
   DW_MULTI_CASES(X)

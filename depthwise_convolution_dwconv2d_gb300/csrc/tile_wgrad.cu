@@ -19,6 +19,7 @@
 // tile_wgrad_impl.cuh and are compiled once per storage type.
 #include "plan.h"
 #include "tile_cases.h"
+#include "tile_fit.h"
 
 namespace dwconv {
 namespace tile {
@@ -29,6 +30,8 @@ cudaError_t wgrad_sel_t(const Conv& c, const void* x, const void* gy, float* ws,
 bool wgrad_supported(const Conv& c) {
   if (!c.planes32()) return false;
   if (c.kh != c.kw || c.sh != c.sw || c.dh != c.dw || c.W > 1024 || c.Wo > 1024) return false;
+  const int es = c.dtype == DWCONV_F32 ? 4 : 2;
+  if (wgrad_min_bytes(c.kh, c.sh, c.dh, c.m, c.Wo, es) > 48 * 1024) return false;
 #define X(K, S, D, M) if (c.kh == K && c.sh == S && c.dh == D && c.m == M) return true;
   DW_WGRAD_CASES(X)
 #undef X

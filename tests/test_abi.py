@@ -173,3 +173,23 @@ def test_plane_routing_and_chunking(lib):
         assert ws % per_chunk == 0
         chunks = ws // per_chunk
         assert 1 <= chunks <= N, (N, C, H, s, chunks)
+
+
+def test_tile_routing_respects_band_limits(lib):
+    """A shape whose narrowest tile band would exceed the tile planner's
+    48 KB shared-memory limit is routed to the generic kernels by the host
+    planner, instead of failing at launch. Worked cases (fp32):
+    - 3x3, dilation 5, padding 5, rows of 400: the forward's narrowest band
+      is 20 output rows = 30 input rows x a 416-element pitch x 4 B
+      = 49,920 B;
+    - 3x3, padding 1, multiplier 2, rows of 1024: the stride-1 grad-input
+      stages 2 grad_out planes of 6 rows x 1032 elements x 4 B = 49,536 B."""
+    assert B.dwconv2d_plan_name(B.make_desc(2, 4, 16, 400, 3, 1, 5, 5), 0) == "generic"
+    assert B.dwconv2d_plan_name(B.make_desc(2, 4, 16, 1024, 3, 1, 1, 1, 2), 1) == "generic"
+    # the same filters on narrower rows stay on the tile kernels
+    assert B.dwconv2d_plan_name(B.make_desc(2, 4, 16, 256, 3, 1, 5, 5), 0) == "tile"
+    assert B.dwconv2d_plan_name(B.make_desc(2, 4, 16, 512, 3, 1, 1, 1, 2), 1) == "tile"
+    # the fused multi-dilation path fits its 96 KB bands up to its 512-wide rows
+    ds = [B.make_desc(2, 8, 16, 512, 3, 1, d, d, out_c_offset=8 * i, out_c_total=24)
+          for i, d in enumerate((1, 3, 5))]
+    assert B.dwconv2d_multi_plan_name(ds) == "tile"
