@@ -26,6 +26,24 @@ bool supported(const Conv& c) {
   return true;
 }
 
+// The weight gradient stages an x tile and a grad_out plane per stage, two
+// stages, plus per-group sums (fp32, whatever the storage type); its planner
+// gives up above 220 KB, which large planes with large filters exceed (k = 31
+// from about 96 x 96). This is the same arithmetic, on the shape alone.
+bool wgrad_supported(const Conv& c) {
+  if (!supported(c)) return false;
+  const int64_t K = c.kh, R = 4, V = 4, nt = 256;
+  auto rup4 = [](int64_t v) { return (v + 3) / 4 * 4; };
+  const int64_t gpitch = rup4(c.Wo);
+  int64_t xpitch = rup4((K + V - 1) / V * V + gpitch + 4);
+  if (xpitch < c.W + c.pw) xpitch = rup4(c.W + c.pw);
+  const int64_t stage = rup4((c.Ho + K - 1) * xpitch + c.Ho * gpitch);
+  const int64_t items = ((K + R - 1) / R) * ((K + V - 1) / V);
+  if (items > nt) return false;
+  const int64_t G = items >= nt ? 1 : nt / items;
+  return (2 * stage + G * (K * K + 1) + nt / 32) * 4 <= 220 * 1024;
+}
+
 cudaError_t fwd(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s) {
   cudaError_t e = cudaErrorInvalidConfiguration;
   DWCONV_DISPATCH_DTYPE(c.dtype, T, e = fwd_t<T>(c, x, w, b, y, s));

@@ -56,7 +56,7 @@ Algo plan_bwd_data(const Conv& c) {
 WPlan plan_bwd_weight(const Conv& c) {
   if (!force_generic() && plane::wgrad_supported(c)) return WPlan{Algo::Plane, plane::wgrad_chunks(c)};
   if (!force_generic() && tile::wgrad_supported(c)) return WPlan{Algo::Tile, tile::wgrad_chunks(c)};
-  if (!force_generic() && large::supported(c)) return WPlan{Algo::Large, large::wgrad_chunks(c)};
+  if (!force_generic() && large::wgrad_supported(c)) return WPlan{Algo::Large, large::wgrad_chunks(c)};
   // generic first pass: a chunk of whole samples per block, at most 2^20
   // positions per chunk so each thread's serial chain stays <= 4096 terms.
   const int64_t hw = c.Ho * c.Wo;

@@ -63,6 +63,7 @@ Algo plan_multi(int nb, const Conv* cs);
 namespace large {
 // large.cu: large-kernel direct convolution (fp32 FMA), stride 1
 bool supported(const Conv& c);
+bool wgrad_supported(const Conv& c);  // supported() and the weight-gradient stages fit shared memory
 cudaError_t fwd(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s);
 cudaError_t bwd_data(const Conv& c, const void* gy, const void* w, void* gx, bool acc, cudaStream_t s);
 int wgrad_chunks(const Conv& c);

@@ -193,3 +193,16 @@ def test_tile_routing_respects_band_limits(lib):
     ds = [B.make_desc(2, 8, 16, 512, 3, 1, d, d, out_c_offset=8 * i, out_c_total=24)
           for i, d in enumerate((1, 3, 5))]
     assert B.dwconv2d_multi_plan_name(ds) == "tile"
+
+
+def test_large_weight_gradient_routing_respects_shared_memory(lib):
+    """The large-filter weight gradient stages two fp32 (x tile + grad_out
+    plane) stages; from 112 x 112 planes it would need more than its 220 KB
+    limit (k = 9 at 112 x 112: 2 x 27,904 floats + 28 group sums of 82 floats
+    + 8 = 232 KB), so those shapes take the generic weight gradient while the
+    forward and grad-input stay on the large kernels."""
+    big = B.make_desc(4, 8, 112, 112, 9, 1, 4)
+    assert B.dwconv2d_plan_name(big, 0) == "large"
+    assert B.dwconv2d_plan_name(big, 2) == "generic"
+    fits = B.make_desc(4, 8, 96, 96, 31, 1, 15)
+    assert B.dwconv2d_plan_name(fits, 2) == "large"
