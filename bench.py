@@ -2,18 +2,31 @@
 """Benchmark: one step = forward, backward-data and backward-weight of every
 layer of a synthetic depthwise workload, through libdwconv's C ABI.
 
-Default workload: the MobileNet layer table of "Spatial Depthwise
-Convolution on the GPU #3057" at batch 64 (3x3, pad 1, stride 1/2, fp32).
+The five workloads (``depthwise_convolution_dwconv2d_gb300.workloads``):
+  pr1        -- N=1 C=32 28x28 3x3 fp32 ("Spatial Depthwise Convolution on
+                the GPU #3057", its smallest MobileNet layer);
+  mobilenet  -- the PR's MobileNet layer table at batch 64, fp32;
+  largek     -- 64 x 384 x {32,48,64}^2, k in {7,13,21,27,31}, fp32 and fp16
+                (the MegEngine large-kernel article's setting);
+  multidil   -- three 3x3 branches with dilation 1/3/5 into one concatenated
+                output, bf16 (the DynamicConvolutionOperator README);
+  multiplier -- 128 x 256 x 28^2, 5x5, multiplier 2, bias, bf16.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                    [--workload mobilenet|pr1|largek|multidil|multiplier]
+                    [--workload all|pr1|mobilenet|largek|multidil|multiplier]
 
-Prints ONE JSON line (rank 0). ``value`` is algorithmic bytes moved per
-second (GB/s, whole job), with every input resident in HBM and L2 flushed
-before every call; ``e2e`` is the same metric with pinned host buffers
-copied in and results copied out inside the timed region. ``--impl
-reference`` times the fp64 CPU oracle on a bounded sample of the same
-workload instead (the only reference that exists for this method).
+With no flags every workload is timed, one after another, and ONE JSON line
+is printed (rank 0). Its headline (``value``, ``config``, ``roofline``,
+``e2e``, ``cpu_baseline``) is the large-kernel sweep, in TFLOP/s of
+valid-tap FMAs (the largest workload, and the compute-bound one);
+``configs`` holds a record per workload with ms, GB/s, TFLOP/s, a roofline
+for every kernel family, an end-to-end figure and the oracle's CPU time.
+``value`` is measured with every input resident in HBM and L2 flushed before
+every call; ``e2e`` is the same metric with pinned host buffers copied in and
+results copied out inside the timed region (copies on two side streams,
+overlapped with the compute of other layers). ``--impl reference`` times the
+fp64 CPU oracle on a bounded sample of the headline workload instead (the
+only reference that exists for this method).
 """
 from __future__ import annotations
 
@@ -21,6 +34,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -33,14 +47,30 @@ sys.path.insert(0, ROOT)
 METRIC = "dwconv fwd/bwd-data/bwd-weight ms, achieved GB/s or TFLOP/s vs roofline"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+ORDER = ("pr1", "mobilenet", "largek", "multidil", "multiplier")
+HEADLINE = "largek"
 WORKLOAD_TEXT = {
+    "pr1": "PR1 layer, fp32 NCHW, N=1 C=32 H=W=28, 3x3, stride 1, pad 1, fwd+bwd_data+bwd_weight",
     "mobilenet": "MobileNet-shape sweep, fp32 NCHW, N=64, 3x3 pad 1, multiplier 1, fwd+bwd_data+bwd_weight; "
                  "layers (C,H=W,stride): (64,112,2),(128,56,1),(128,56,2),(256,28,1),(256,28,2),(512,14,1),"
                  "(512,14,2),(1024,7,2)",
-    "pr1": "PR1 layer, fp32 NCHW, N=1 C=32 H=W=28, 3x3, stride 1, pad 1",
-    "largek": "Large-kernel depthwise, N=64 C=384, H=W in {32,48,64}, k in {7,13,21,27,31}, stride 1, pad k//2, fp32 and fp16",
-    "multidil": "Fused multi-dilation branches, bf16, N=2 C=64 H=W=256, 3x3 dilation 1,3,5 into one N x 3C x H x W output",
-    "multiplier": "Depth-multiplier layer, bf16, N=128 C=256 H=W=28, m=2, 5x5 pad 2, bias",
+    "largek": "Large-kernel depthwise, N=64 C=384, H=W in {32,48,64}, k in {7,13,21,27,31}, stride 1, pad k//2, "
+              "fp32 and fp16 (fp32 accumulation), fwd+bwd_data+bwd_weight",
+    "multidil": "Fused multi-dilation branches, bf16, N=2 C=64 H=W=256, 3x3 dilation 1,3,5 (pad = dilation) into "
+                "one N x 3C x H x W output; fwd + bwd_data (branch sum) + bwd_weight per branch",
+    "multiplier": "Depth-multiplier layer, bf16, N=128 C=256 H=W=28, m=2 (512 out channels), 5x5 pad 2, bias; "
+                  "fwd+bwd_data+bwd_weight+bias grad",
+}
+# Source files whose device code each kernel family runs: a committed DRAM
+# traffic figure is reported only while these files are unchanged.
+FAMILY_SOURCES = {
+    "tile": ("common.cuh", "plan.h", "tile.cuh", "tile_plan.cuh", "tile_fit.h", "tile_cases.h", "tma.cuh",
+             "tile_fwd.cu", "tile_fwd_impl.cuh", "tile_bwd2.cu", "tile_bwd2_impl.cuh", "tile_wgrad.cu",
+             "tile_wgrad_impl.cuh", "tile_multi.cu", "generic.cu"),
+    "plane": ("common.cuh", "plan.h", "plane.cu", "generic.cu"),
+    "large": ("common.cuh", "plan.h", "tile.cuh", "large.cu", "large_impl.cuh", "generic.cu"),
+    "ibgemm": ("common.cuh", "plan.h", "tma.cuh", "tma.cu", "ibgemm.cu"),
+    "generic": ("common.cuh", "plan.h", "generic.cu"),
 }
 
 
@@ -98,20 +128,40 @@ def layer_calls(item):
 
 # ------------------------------------------------------------------ helpers
 def load_peaks():
+    """(HBM GB/s, its source, dense bf16 TFLOP/s burst, its source)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    hbm, hk, tc, tk = FALLBACK_HBM_GBS, "fallback", FALLBACK_BF16_TFLOPS, "fallback"
     if os.path.exists(path):
         try:
             j = json.load(open(path))
-            hbm = j.get("hbm_gbs") or j.get("hbm_GBps")
-            if hbm:
-                return float(hbm), "measured", j
+            if j.get("hbm_gbs"):
+                hbm, hk = float(j["hbm_gbs"]), "measured"
+            if j.get("bf16_tflops"):
+                tc, tk = float(j["bf16_tflops"]), "measured"
         except Exception:
             pass
-    return FALLBACK_HBM_GBS, "fallback", None
+    return hbm, hk, tc, tk
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.processor() or platform.machine()
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled while the timed loop runs."""
+    """nvidia-smi clocks and throttle reasons, sampled while a timed loop runs."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -145,49 +195,52 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
-            except ValueError:
-                continue
-            for nm, v in zip(names, parts[4:8]):
-                if v.lower() == "active":
-                    reasons.add(nm)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+
+def clock_summary(lines):
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for ln in lines:
+        parts = [p.strip() for p in ln.split(",")]
+        if len(parts) < 8:
+            continue
+        try:
+            sm.append(float(parts[0]))
+            mx.append(float(parts[1]))
+        except ValueError:
+            continue
+        for nm, v in zip(names, parts[4:8]):
+            if v.lower() == "active":
+                reasons.add(nm)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+            "reasons": sorted(reasons)}
 
 
-def csrc_digest():
+def family_digest(family):
     h = hashlib.sha256()
     d = os.path.join(ROOT, "depthwise_convolution_dwconv2d_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    for f in FAMILY_SOURCES.get(family, ()):
+        p = os.path.join(d, f)
         h.update(f.encode())
-        h.update(open(os.path.join(d, f), "rb").read())
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel_key):
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
-    the current kernel sources; else None."""
+def ncu_traffic(key, family):
+    """Per-launch DRAM bytes of one kernel family from the committed ncu
+    figures, if they were taken on the family's current sources; else None."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
     try:
-        j = json.load(open(path))
+        e = json.load(open(path)).get("kernels", {}).get(key)
     except Exception:
         return None
-    if j.get("csrc_digest") != csrc_digest():
+    if not e or e.get("digest") != family_digest(family):
         return None
-    return j.get("per_launch_bytes", {}).get(kernel_key)
+    return e.get("bytes_per_launch")
 
 
 def fma_probe_tflops(dev, stream):
@@ -199,46 +252,49 @@ def fma_probe_tflops(dev, stream):
     for _ in range(2):
         B.dwconv_fma_probe(152 * 8, 4096, sink, stream)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    B.dwconv_fma_probe(152 * 8, 16384, sink, stream)
-    b.record(stream)
-    torch.cuda.synchronize()
-    return 2 * 16 * 16384 * 152 * 8 * 256 / a.elapsed_time(b) / 1e9
+    best = 0.0
+    for _ in range(3):
+        a.record(stream)
+        B.dwconv_fma_probe(152 * 8, 16384, sink, stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        best = max(best, 2 * 16 * 16384 * 152 * 8 * 256 / a.elapsed_time(b) / 1e9)
+    return best
 
 
 # ------------------------------------------------------------------ CPU oracle
 def oracle_sample(items, budget_s):
-    """Time the fp64 oracle on the first n samples of every layer; n grows
-    until one pass over the sample takes about budget_s. Returns
-    (bytes/s, fma/s, seconds, n, description)."""
-    import numpy as np
+    """Time the fp64 oracle on a bounded sample of every layer: the first n
+    samples and, while even one sample takes longer than the budget, the
+    first c channels. Returns (bytes/s, fma/s, seconds, description)."""
     import oracle
     from depthwise_convolution_dwconv2d_gb300 import workloads as WL
     oracle.build()
 
-    def run(n):
+    def run(n, c_cap):
         t_total, bytes_total, fma_total = 0.0, 0, 0
         for item in items:
+            C = min(item.C, c_cap)
             if isinstance(item, WL.Multi):
                 brs, ctot = item.branches()
-                sub = WL.Multi(N=n, C=item.C, H=item.H, W=item.W, dilations=item.dilations, k=item.k,
+                sub = WL.Multi(N=n, C=C, H=item.H, W=item.W, dilations=item.dilations, k=item.k,
                                dtype=item.dtype, x_dist=item.x_dist, w_std=item.w_std)
-                sbrs, _ = sub.branches()
-                inp = WL.make_inputs(sbrs[0], gy_channels=ctot)
+                sbrs, sctot = sub.branches()
+                x, gy = WL.make_x(sbrs[0]), WL.make_gy(sbrs[0], gy_channels=sctot)
+                ws = [WL.make_w(L, branch=i).f64 for i, L in enumerate(sbrs)]
                 cvs = [oracle.Conv(N=n, C=L.C, H=L.H, W=L.W, kh=L.k, kw=L.k, sh=L.s, sw=L.s, ph=L.p, pw=L.p,
-                                   dh=L.d, dw=L.d, off=i * L.C, c_total=ctot) for i, L in enumerate(sbrs)]
-                ws = [inp.w.f64] * len(cvs)
+                                   dh=L.d, dw=L.d, off=i * L.C, c_total=sctot) for i, L in enumerate(sbrs)]
                 t0 = time.perf_counter()
-                oracle.fwd_multi(cvs, inp.x.f64, ws)
-                oracle.bwd_data_multi(cvs, inp.gy.f64, ws)
+                oracle.fwd_multi(cvs, x.f64, ws)
+                oracle.bwd_data_multi(cvs, gy.f64, ws)
                 for cv in cvs:
-                    oracle.bwd_weight(cv, inp.x.f64, inp.gy.f64)
+                    oracle.bwd_weight(cv, x.f64, gy.f64)
                 t_total += time.perf_counter() - t0
                 for _, b, f, _ in layer_calls(sub):
                     bytes_total += b
                     fma_total += f
                 continue
-            L = WL.Layer(**{**item.__dict__, "N": n})
+            L = WL.Layer(**{**item.__dict__, "N": n, "C": C})
             inp = WL.make_inputs(L)
             cv = oracle.Conv(N=n, C=L.C, H=L.H, W=L.W, kh=L.k, kw=L.k, sh=L.s, sw=L.s, ph=L.p, pw=L.p,
                              dh=L.d, dw=L.d, m=L.m)
@@ -253,115 +309,172 @@ def oracle_sample(items, budget_s):
                 fma_total += f
         return t_total, bytes_total, fma_total
 
+    full_c = max(i.C for i in items)
+    full_n = min(i.N for i in items)
+    c = min(full_c, 32)
+    t, by, fm = run(1, c)
     n = 1
-    t, by, fm = run(1)
-    full_n = min(getattr(i, "N", 1) for i in items)
-    if t < budget_s and full_n > 1:
-        n = max(1, min(full_n, int(budget_s / max(t, 1e-3))))
-        if n > 1:
-            t, by, fm = run(n)
-    desc = f"first {n} sample(s) of every layer, fwd+bwd_data+bwd_weight, one timed pass"
-    return by / t, fm / t, t, n, desc
+    if t < budget_s / 2:
+        # grow the channel count first, then the batch
+        scale = budget_s / max(t, 1e-3)
+        if c * scale < full_c:
+            c = max(c, int(c * scale) // 8 * 8)
+        else:
+            scale /= full_c / c
+            c = full_c
+            n = max(1, min(full_n, int(scale)))
+        t, by, fm = run(n, c)
+    desc = (f"first {n} sample(s)" + ("" if c >= full_c else f" and first {c} channels") +
+            " of every layer, fwd+bwd_data+bwd_weight, one timed pass")
+    return by / t, fm / t, t, desc
+
+
+def cpu_baseline(name, items, budget_s, unit):
+    import oracle
+    bps, fps, t, desc = oracle_sample(items, budget_s)
+    v = 2 * fps / 1e12 if unit == "TFLOP/s" else bps / 1e9
+    return {"value": round(v, 5), "unit": unit, "cores": oracle.num_threads(), "cpu_model": cpu_model(),
+            "kind": "oracle", "sample": desc, "seconds": round(t, 2),
+            "GBps": round(bps / 1e9, 4), "tflops_valid": round(2 * fps / 1e12, 6)}
 
 
 # ------------------------------------------------------------------ GPU arm
-def gpu_arm(args, rank, world):
-    import numpy as np
+class HostCache:
+    """Synthetic host tensors, drawn once per (shape, dtype, stream, std) and
+    pinned; layers with equal shapes share them (the device buffers are still
+    one per layer)."""
+
+    def __init__(self):
+        self.t = {}
+
+    def get(self, key, make):
+        if key not in self.t:
+            import torch
+            import numpy as np
+            st = make()
+            if st.dtype == "bf16":
+                h = torch.from_numpy(st.store.view(np.int16)).view(torch.bfloat16)
+            else:
+                h = torch.from_numpy(st.store)
+            self.t[key] = h.pin_memory()
+        return self.t[key]
+
+
+def setup_workload(name, items, dev, stream, hc, out_host):
+    """Device buffers and the call list of one step. Returns (calls, groups):
+    calls = [(pass, label, family, bytes, fma, launches, fn)], groups = one
+    per layer: (h2d pairs, call indices, d2h pairs)."""
     import torch
-    from depthwise_convolution_dwconv2d_gb300 import binding as B, build as BLD, workloads as WL
-
-    BLD.build()
-    B.load()
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    stream = torch.cuda.current_stream()
-    items = build_workload(args.workload)
-    if args.layers:
-        keep = set(args.layers.split(","))
-        items = [i for i in items if i.label() in keep]
-        if not items:
-            raise SystemExit(f"--layers matched nothing in {args.workload}")
-    if args.batch:
-        # smaller batch of the same layers (profiling runs only)
-        items = [type(i)(**{**i.__dict__, "N": args.batch}) for i in items]
-    dist = None
-    if world > 1:
-        import torch.distributed as dist_
-        dist = dist_
-
-    def dev_tensor(t, pinned=False):
-        if t.dtype == "bf16":
-            h = torch.from_numpy(t.store.view(np.int16).copy()).view(torch.bfloat16)
-        else:
-            h = torch.from_numpy(np.ascontiguousarray(t.store))
-        if pinned:
-            h = h.pin_memory()
-        return h.to(dev), h
+    from depthwise_convolution_dwconv2d_gb300 import binding as B, workloads as WL
 
     def tdt(dt):
         return {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[dt]
 
-    # build device buffers and the call list of one step
-    calls = []   # (pass, label, bytes, fma, launches, fn)
-    h2d, d2h = [], []   # (host, device) pairs for the end-to-end run
+    def host_out(t):
+        key = (tuple(t.shape), t.dtype)
+        if key not in out_host:
+            out_host[key] = torch.empty(t.shape, dtype=t.dtype, device="cpu").pin_memory()
+        return out_host[key]
+
+    def fam(plan, dt):
+        return f"{plan}:{dt}"
+
+    calls, groups = [], []
     for item in items:
         if isinstance(item, WL.Multi):
             brs, ctot = item.branches()
-            inp = WL.make_inputs(brs[0], gy_channels=ctot)
-            from depthwise_convolution_dwconv2d_gb300 import synth
-            wts = [inp.w] + [synth.normal_tensor((item.C, item.k, item.k), item.dtype, 0,
-                                                  synth.STREAM_W + 16 * i, std=item.w_std)
-                             for i in range(1, len(brs))]
-            x, xh = dev_tensor(inp.x, True)
-            gy, gyh = dev_tensor(inp.gy, True)
-            wd = [dev_tensor(w, True) for w in wts]
+            L0 = brs[0]
+            xd = "uniform" if item.x_dist == "uniform" else "normal"
+            xh = hc.get(("x", (item.N, item.C, item.H, item.W), item.dtype, xd), lambda: WL.make_x(L0))
+            gyh = hc.get(("gy", (item.N, ctot, L0.Ho, L0.Wo), item.dtype),
+                         lambda: WL.make_gy(L0, gy_channels=ctot))
+            whs = [hc.get(("w", (item.C, item.k, item.k), item.dtype, i, item.w_std),
+                          lambda i=i: WL.make_w(brs[i], branch=i))
+                   for i in range(len(brs))]
+            x, gy = xh.to(dev), gyh.to(dev)
+            wdev = [h.to(dev) for h in whs]
             descs = [B.make_desc(**L.desc_kwargs(), out_c_offset=i * item.C, out_c_total=ctot)
                      for i, L in enumerate(brs)]
-            y = torch.empty((item.N, ctot, item.H, item.W), dtype=tdt(item.dtype), device=dev)
+            y = torch.empty((item.N, ctot, L0.Ho, L0.Wo), dtype=tdt(item.dtype), device=dev)
             gx = torch.empty((item.N, item.C, item.H, item.W), dtype=tdt(item.dtype), device=dev)
             gws = [torch.empty((item.C, item.k, item.k), dtype=tdt(item.dtype), device=dev) for _ in brs]
             wss = [torch.empty(B.dwconv2d_bwd_weight_workspace_size(dd) // 4 + 4, device=dev) for dd in descs]
-            h2d += [(xh, x), (gyh, gy)] + [(h, dd) for dd, h in wd]
-            d2h += [(y, torch.empty_like(y, device="cpu").pin_memory()),
-                    (gx, torch.empty_like(gx, device="cpu").pin_memory())]
-            d2h += [(g, torch.empty_like(g, device="cpu").pin_memory()) for g in gws]
-            wdev = [dd for dd, _ in wd]
             cl = layer_calls(item)
             nb = len(brs)
-            fused = B.dwconv2d_multi_plan_name(descs) == "tile"
-            calls.append(("fwd", item.label(), cl[0][1], cl[0][2], 1 if fused else nb,
+            mplan = B.dwconv2d_multi_plan_name(descs)
+            fused = mplan == "tile"
+            idx0 = len(calls)
+            calls.append(("fwd", item.label(), fam("multi-" + mplan, item.dtype), cl[0][1], cl[0][2],
+                          1 if fused else nb,
                           lambda descs=descs, x=x, wdev=wdev, y=y: B.dwconv2d_fwd_multi(descs, x, wdev, None, y, stream)))
-            calls.append(("bwd_data", item.label(), cl[1][1], cl[1][2], 1,
+            calls.append(("bwd_data", item.label(), fam("multi-" + mplan, item.dtype), cl[1][1], cl[1][2], 1,
                           lambda descs=descs, gy=gy, wdev=wdev, gx=gx: B.dwconv2d_bwd_data_multi(descs, gy, wdev, gx, stream)))
             for i, dd in enumerate(descs):
-                calls.append(("bwd_weight", f"{item.label()}_br{i}", cl[2 + i][1], cl[2 + i][2], 2,
+                calls.append(("bwd_weight", f"{item.label()}_br{i}", fam(B.dwconv2d_plan_name(dd, 2), item.dtype),
+                              cl[2 + i][1], cl[2 + i][2], 2,
                               lambda dd=dd, x=x, gy=gy, g=gws[i], ws=wss[i]: B.dwconv2d_bwd_weight(dd, x, gy, g, None, ws, None, stream)))
+            h2d = [(xh, x), (gyh, gy)] + list(zip(whs, wdev))
+            d2h = [(t, host_out(t)) for t in [y, gx] + gws]
+            groups.append((h2d, list(range(idx0, len(calls))), d2h))
             continue
         L = item
-        inp = WL.make_inputs(L)
+        xd = "uniform" if L.x_dist == "uniform" else "normal"
+        wstd = L.w_std if L.w_std is not None else 1.0 / L.k
+        xh = hc.get(("x", (L.N, L.C, L.H, L.W), L.dtype, xd), lambda L=L: WL.make_x(L))
+        wh = hc.get(("w", (L.OC, L.k, L.k), L.dtype, 0, wstd), lambda L=L: WL.make_w(L))
+        gyh = hc.get(("gy", (L.N, L.OC, L.Ho, L.Wo), L.dtype), lambda L=L: WL.make_gy(L))
+        bh = hc.get(("b", (L.OC,), L.dtype, L.b_std), lambda L=L: WL.make_b(L)) if L.bias else None
         d = B.make_desc(**L.desc_kwargs())
-        x, xh = dev_tensor(inp.x, True)
-        w, wh = dev_tensor(inp.w, True)
-        gy, gyh = dev_tensor(inp.gy, True)
-        b, bh = dev_tensor(inp.b, True) if inp.b is not None else (None, None)
+        x, w, gy = xh.to(dev), wh.to(dev), gyh.to(dev)
+        b = bh.to(dev) if bh is not None else None
         y = torch.empty((L.N, L.OC, L.Ho, L.Wo), dtype=tdt(L.dtype), device=dev)
         gx = torch.empty((L.N, L.C, L.H, L.W), dtype=tdt(L.dtype), device=dev)
         gw = torch.empty((L.OC, L.k, L.k), dtype=tdt(L.dtype), device=dev)
         gb = torch.empty((L.OC,), dtype=tdt(L.dtype), device=dev) if L.bias else None
         ws = torch.empty(B.dwconv2d_bwd_weight_workspace_size(d) // 4 + 4, device=dev)
-        h2d += [(xh, x), (wh, w), (gyh, gy)] + ([(bh, b)] if b is not None else [])
-        d2h += [(t, torch.empty_like(t, device="cpu").pin_memory()) for t in (y, gx, gw, gb) if t is not None]
         cl = layer_calls(L)
-        calls.append(("fwd", L.label(), cl[0][1], cl[0][2], 1,
+        idx0 = len(calls)
+        calls.append(("fwd", L.label(), fam(B.dwconv2d_plan_name(d, 0), L.dtype), cl[0][1], cl[0][2], 1,
                       lambda d=d, x=x, w=w, b=b, y=y: B.dwconv2d_fwd(d, x, w, b, y, stream)))
-        calls.append(("bwd_data", L.label(), cl[1][1], cl[1][2], 1,
+        calls.append(("bwd_data", L.label(), fam(B.dwconv2d_plan_name(d, 1), L.dtype), cl[1][1], cl[1][2], 1,
                       lambda d=d, gy=gy, w=w, gx=gx: B.dwconv2d_bwd_data(d, gy, w, gx, 0, stream)))
-        calls.append(("bwd_weight", L.label(), cl[2][1], cl[2][2], 2,
+        calls.append(("bwd_weight", L.label(), fam(B.dwconv2d_plan_name(d, 2), L.dtype), cl[2][1], cl[2][2], 2,
                       lambda d=d, x=x, gy=gy, gw=gw, gb=gb, ws=ws: B.dwconv2d_bwd_weight(d, x, gy, gw, gb, ws, None, stream)))
+        h2d = [(xh, x), (wh, w), (gyh, gy)] + ([(bh, b)] if b is not None else [])
+        d2h = [(t, host_out(t)) for t in (y, gx, gw, gb) if t is not None]
+        groups.append((h2d, list(range(idx0, len(calls))), d2h))
+    return calls, groups
 
-    step_bytes = sum(c[2] for c in calls)
-    step_fma = sum(c[3] for c in calls)
-    launches_per_step = sum(c[4] for c in calls)
+
+def roofline_of(fam_rec, bound_peaks, hbm_peak, hbm_kind, traffic):
+    """Roofline of one kernel family: t_roof = max(bytes / HBM peak, FLOPs /
+    compute peak), frac = t_roof / t_measured; achieved in the bound's unit."""
+    ms, by, fma = fam_rec["ms"], fam_rec["bytes"], fam_rec["fma"]
+    comp_kind, comp_peak, comp_src = bound_peaks
+    t_mem = by / (hbm_peak * 1e6)           # ms
+    t_cmp = 2 * fma / (comp_peak * 1e9)     # ms
+    if t_cmp > t_mem:
+        ach = 2 * fma / ms / 1e9
+        return {"bound": comp_kind, "achieved": round(ach, 2), "peak": round(comp_peak, 1), "unit": "TFLOP/s",
+                "frac": round(ach / comp_peak, 4), "peak_source": comp_src, "work": "valid-tap FMAs x 2",
+                "traffic": traffic, "hbm_frac": round(by / ms / 1e6 / hbm_peak, 4)}
+    ach = by / ms / 1e6
+    return {"bound": "hbm", "achieved": round(ach, 1), "peak": round(hbm_peak, 1), "unit": "GB/s",
+            "frac": round(ach / hbm_peak, 4),
+            "peak_source": f"{hbm_kind} ({'MEASURED_PEAKS.json hbm_gbs' if hbm_kind == 'measured' else 'profiling recipe fallback 6.8 TB/s'})",
+            "work": "algorithmic bytes", "traffic": traffic,
+            "compute_frac": round(2 * fma / ms / 1e9 / comp_peak, 4)}
+
+
+def time_workload(name, items, args, dev, stream, world, dist, peaks, fma_tflops):
+    import torch
+    from depthwise_convolution_dwconv2d_gb300 import binding as B
+    hc, out_host = HostCache(), {}
+    calls, groups = setup_workload(name, items, dev, stream, hc, out_host)
+    torch.cuda.synchronize()
+    step_bytes = sum(c[3] for c in calls)
+    step_fma = sum(c[4] for c in calls)
+    launches_per_step = sum(c[5] for c in calls)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     # L2 flush before every timed call: write a buffer of 2x L2 (evicts the
     # inputs), then read a second, clean 2x L2 buffer, so the write-back of
@@ -380,10 +493,9 @@ def gpu_arm(args, rank, world):
         if dist is not None:
             dist.barrier()
 
-    # warm-up
     for _ in range(args.warmup):
         for c in calls:
-            c[5]()
+            c[6]()
     torch.cuda.synchronize()
 
     # timed: K steps, L2 flushed before every call, per-call events
@@ -398,164 +510,218 @@ def gpu_arm(args, rank, world):
             for i, c in enumerate(calls):
                 flush_l2()
                 ev[k][i][0].record(stream)
-                c[5]()
+                c[6]()
                 ev[k][i][1].record(stream)
         torch.cuda.synchronize()
         barrier()
         t_wall = time.perf_counter() - t_wall0
     per_call = [[ev[k][i][0].elapsed_time(ev[k][i][1]) for i in range(len(calls))] for k in range(args.steps)]
-    step_ms = [sum(r) for r in per_call]
-    ms_per_step = statistics.mean(step_ms)
+    ms_per_step = statistics.mean(sum(r) for r in per_call)
 
-    # end to end: pinned host inputs -> device, the step, results -> pinned host
-    e2e_ms = None
+    # end to end: per layer, inputs copied from pinned host memory on one side
+    # stream, the layer's calls on the compute stream, its results copied back
+    # on another side stream; layer i's copies overlap other layers' compute
+    e2e_ms, h2d_bytes, d2h_bytes = None, 0, 0
     if not args.no_e2e:
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        g_in = [torch.cuda.Event() for _ in groups]
+        g_cmp = [torch.cuda.Event() for _ in groups]
+        g_out = [torch.cuda.Event() for _ in groups]
+        started = [False] * len(groups)
+
+        def e2e_step():
+            for gi, (h2d, idxs, d2h) in enumerate(groups):
+                if started[gi]:
+                    s_in.wait_event(g_cmp[gi])      # inputs are free once last step's calls ran
+                with torch.cuda.stream(s_in):
+                    for hsrc, ddst in h2d:
+                        ddst.copy_(hsrc, non_blocking=True)
+                g_in[gi].record(s_in)
+                stream.wait_event(g_in[gi])
+                if started[gi]:
+                    stream.wait_event(g_out[gi])    # outputs are free once last step's copies ran
+                for i in idxs:
+                    calls[i][6]()
+                g_cmp[gi].record(stream)
+                s_out.wait_event(g_cmp[gi])
+                with torch.cuda.stream(s_out):
+                    for dsrc, hdst in d2h:
+                        hdst.copy_(dsrc, non_blocking=True)
+                g_out[gi].record(s_out)
+                started[gi] = True
+
         for _ in range(max(1, min(args.warmup, 2))):
-            for hsrc, ddst in h2d:
-                ddst.copy_(hsrc, non_blocking=True)
-            for c in calls:
-                c[5]()
-            for dsrc, hdst in d2h:
-                hdst.copy_(dsrc, non_blocking=True)
+            e2e_step()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ke = max(1, min(args.steps, 10))
         barrier()
         torch.cuda.synchronize()
         e0.record(stream)
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
         for _ in range(ke):
-            for hsrc, ddst in h2d:
-                ddst.copy_(hsrc, non_blocking=True)
-            for c in calls:
-                c[5]()
-            for dsrc, hdst in d2h:
-                hdst.copy_(dsrc, non_blocking=True)
+            e2e_step()
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
         e2e_ms = e0.elapsed_time(e1) / ke
-    h2d_bytes = sum(h.numel() * h.element_size() for h, _ in h2d)
-    d2h_bytes = sum(h.numel() * h.element_size() for _, h in d2h)
+        h2d_bytes = sum(h.numel() * h.element_size() for g in groups for h, _ in g[0])
+        d2h_bytes = sum(h.numel() * h.element_size() for g in groups for _, h in g[2])
 
-    # max over ranks
     if dist is not None:
         t = torch.tensor([ms_per_step, e2e_ms or 0.0], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_per_step, e2e_ms = float(t[0]), (float(t[1]) or None)
 
-    # per pass family: total time and bytes across the step (mean over steps)
-    fam = {}
+    hbm_peak, hbm_kind, tc_peak, tc_kind = peaks
+    fams = {}
+    passes = {}
     for i, c in enumerate(calls):
-        f = fam.setdefault(c[0], {"ms": 0.0, "bytes": 0, "fma": 0, "launches": 0, "calls": 0})
-        f["ms"] += statistics.mean(per_call[k][i] for k in range(args.steps))
-        f["bytes"] += c[2]
-        f["fma"] += c[3]
-        f["launches"] += c[4]
-        f["calls"] += 1
+        ms = statistics.mean(per_call[k][i] for k in range(args.steps))
+        for key, dct in ((f"{c[0]}:{c[2]}", fams), (c[0], passes)):
+            f = dct.setdefault(key, {"ms": 0.0, "bytes": 0, "fma": 0, "launches": 0, "calls": 0})
+            f["ms"] += ms
+            f["bytes"] += c[3]
+            f["fma"] += c[4]
+            f["launches"] += c[5]
+            f["calls"] += 1
     per_layer = {}
     for i, c in enumerate(calls):
         ms = statistics.median(per_call[k][i] for k in range(args.steps))
-        per_layer.setdefault(c[1], {})[c[0]] = {"us": round(ms * 1e3, 2), "GBps": round(c[2] / ms / 1e6, 1),
-                                                "TFLOPs": round(2 * c[3] / ms / 1e9, 2)}
-    peak, peak_kind, _ = load_peaks()
-    dom = max(fam, key=lambda k: fam[k]["ms"])
-    fd = fam[dom]
-    tr = ncu_traffic(f"{args.workload}:{dom}")
-    # the large-kernel sweep is bound by fp32 FMA throughput (its dominant
-    # pass, the weight gradient, runs on the FMA pipes for every dtype);
-    # everything else is bound by HBM bandwidth
-    compute_bound = args.workload == "largek"
-    fma_tflops = None
-    if args.fma_probe or compute_bound:
-        fma_tflops = fma_probe_tflops(dev, stream)
-    if compute_bound:
-        achieved = 2 * fd["fma"] / fd["ms"] / 1e9
-        roof = {"bound": "alu", "kernel": f"{dom} ({fd['calls']} calls, {fd['launches']} launches per step)",
-                "achieved": round(achieved, 2), "peak": round(fma_tflops, 2), "unit": "TFLOP/s",
-                "frac": round(achieved / fma_tflops, 4),
-                "peak_source": "measured in this run (register-only FP32 FMA probe, dwconv_fma_probe; nominal "
-                               "152 SMs x 128 lanes x 2 FLOP x 2.07 GHz = 80.5 TFLOP/s)",
-                "work": "valid-tap FMAs x 2", "traffic": tr}
-    else:
-        achieved = fd["bytes"] / fd["ms"] / 1e6
-        roof = {"bound": "hbm", "kernel": f"{dom} ({fd['calls']} calls, {fd['launches']} launches per step)",
-                "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "peak_source": f"{peak_kind} ({'MEASURED_PEAKS.json hbm_gbs' if peak_kind == 'measured' else 'profiling recipe fallback 6.8 TB/s'})",
-                "traffic": tr}
-    value = world * step_bytes / ms_per_step / 1e6
-    out = {
-        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None,
-        "dtype": sorted({getattr(i, "dtype", "f32") for i in items})[0] if len(items) else "f32",
-        "data": "synthetic (SplitMix64 + Box-Muller, seed 0)",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload,
-                   **({"layers": args.layers} if args.layers else {}),
-                   **({"batch_override": args.batch} if args.batch else {}),
-                   "parallelism": f"replicas x{world} (no collective)",
-                   "l2": "flushed before every call (2x L2 written, then a clean 2x L2 buffer read: inputs not cached, no dirty lines left); inputs resident in HBM",
-                   "step_bytes": step_bytes, "step_fma_valid": step_fma,
-                   "tflops_valid": round(world * 2 * step_fma / ms_per_step / 1e9, 3)},
-        "roofline": roof,
+        per_layer.setdefault(c[1], {})[c[0]] = {"plan": c[2].split(":")[0], "us": round(ms * 1e3, 2),
+                                                "GBps": round(c[3] / ms / 1e6, 1),
+                                                "TFLOPs": round(2 * c[4] / ms / 1e9, 2)}
+    fma_src = ("measured in this run (register-only FP32 FMA probe, dwconv_fma_probe; nominal "
+               "152 SMs x 128 lanes x 2 FLOP x 2.07 GHz = 80.5 TFLOP/s)")
+    tc_src = (f"{tc_kind} ({'MEASURED_PEAKS.json bf16_tflops (dense bf16 burst; fp16 has the same dense rate)' if tc_kind == 'measured' else 'profiling recipe fallback 1.9 PFLOP/s'})")
+    rl = {}
+    for key, f in fams.items():
+        pass_, plan, dt = key.split(":")
+        family = plan.replace("multi-", "")
+        if family == "ibgemm":
+            bp = ("tensor", tc_peak, tc_src)
+        elif fma_tflops:
+            bp = ("alu", fma_tflops, fma_src)
+        else:
+            bp = ("alu", 80.5, "nominal FP32 FMA rate (152 x 128 x 2 x 2.07 GHz)")
+        r = roofline_of(f, bp, hbm_peak, hbm_kind, ncu_traffic(f"{name}:{key}", family))
+        r.update({"kernel": key, "calls": f["calls"], "launches": f["launches"], "ms": round(f["ms"], 4),
+                  "share": round(f["ms"] / ms_per_step, 4)})
+        rl[key] = r
+    dom = max(fams, key=lambda k: fams[k]["ms"])
+    unit = "TFLOP/s" if name == "largek" else "GB/s"
+
+    def metric_of(ms):
+        return (world * 2 * step_fma / ms / 1e9) if unit == "TFLOP/s" else (world * step_bytes / ms / 1e6)
+
+    dts = sorted({getattr(i, "dtype", "f32") for i in items}, key=lambda d: ("f32", "f16", "bf16").index(d))
+    rec = {
+        "workload": WORKLOAD_TEXT[name], "name": name,
+        "value": round(metric_of(ms_per_step), 3), "unit": unit,
+        "ms_per_step": round(ms_per_step, 4),
+        "GBps": round(world * step_bytes / ms_per_step / 1e6, 1),
+        "TFLOPs_valid": round(world * 2 * step_fma / ms_per_step / 1e9, 3),
+        "dtype": "+".join(dts),
+        "step_bytes": step_bytes, "step_fma_valid": step_fma,
+        "roofline": rl[dom],
+        "roofline_by_family": rl,
         "passes": {k: {"ms": round(v["ms"], 4), "GBps": round(v["bytes"] / v["ms"] / 1e6, 1),
-                       "TFLOPs_valid": round(2 * v["fma"] / v["ms"] / 1e9, 3), "launches": v["launches"]}
-                   for k, v in fam.items()},
+                       "TFLOPs_valid": round(2 * v["fma"] / v["ms"] / 1e9, 3), "launches": v["launches"],
+                       "share": round(v["ms"] / ms_per_step, 4)}
+                   for k, v in passes.items()},
         "per_layer": per_layer,
         "gpu_launches": launches_per_step * args.steps,
-        "e2e": ({"value": round(world * step_bytes / e2e_ms / 1e6, 1), "unit": "GB/s",
-                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d_bytes,
-                 "d2h_bytes_per_step": d2h_bytes} if e2e_ms else None),
-        "clocks": clk.summary(),
+        "e2e": ({"value": round(metric_of(e2e_ms), 3), "unit": unit, "ms_per_step": round(e2e_ms, 4),
+                 "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
+                 "copies": "per layer: H2D on one side stream, D2H on another, overlapped with other layers' compute"}
+                if e2e_ms else None),
+        "clocks": clock_summary(clk.lines),
+        "clock_lines": clk.lines,
         "wall_s_timed": round(t_wall, 3),
+        "steps": args.steps,
     }
-    if args.fma_probe or compute_bound:
-        out["fp32_fma_probe_tflops"] = round(fma_tflops, 2)
-    return out, items
+    del calls, groups, hc, out_host, flush, flush_clean
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
+
+
+def gpu_arm(args, names, rank, world):
+    import torch
+    from depthwise_convolution_dwconv2d_gb300 import binding as B, build as BLD
+
+    BLD.build()
+    B.load()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_
+        dist = dist_
+    peaks = load_peaks()
+    fma_tflops = fma_probe_tflops(dev, stream)
+    recs, items_of = {}, {}
+    for name in names:
+        items = build_workload(name)
+        if args.layers:
+            keep = set(args.layers.split(","))
+            items = [i for i in items if i.label() in keep]
+            if not items:
+                continue
+        if args.batch:
+            # smaller batch of the same layers (profiling runs only)
+            items = [type(i)(**{**i.__dict__, "N": args.batch}) for i in items]
+        items_of[name] = items
+        recs[name] = time_workload(name, items, args, dev, stream, world, dist, peaks, fma_tflops)
+    if not recs:
+        raise SystemExit(f"--layers {args.layers} matched nothing")
+    return recs, items_of, fma_tflops, peaks
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=None,
-                    help="timed steps (default: 300 for the MobileNet sweep, so the timed region spans "
-                         "several clock samples; 20 otherwise and for the reference arm)")
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="mobilenet", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--workload", default="all", choices=["all"] + list(ORDER))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--fma-probe", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
     ap.add_argument("--layers", default="", help="comma-separated layer labels to keep (profiling runs)")
     ap.add_argument("--batch", type=int, default=0, help="override the batch size (profiling runs)")
     args = ap.parse_args()
-    if args.steps is None:
-        args.steps = 300 if (args.workload == "mobilenet" and args.impl == "gb300") else 20
+    names = list(ORDER) if args.workload == "all" else [args.workload]
+    head = HEADLINE if HEADLINE in names else names[0]
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
+    unit_of = lambda n: "TFLOP/s" if n == "largek" else "GB/s"
 
     if args.impl == "reference":
         if rank != 0:
             return
-        items = build_workload(args.workload)
+        items = build_workload(head)
         total = max(1, args.steps + args.warmup)
         per_step = max(1.0, min(args.cpu_seconds, 150.0 / total))
-        vals = []
-        n_s, desc, ncores = 0, "", 0
-        import oracle
+        vals, desc, t_all = [], "", 0.0
         for k in range(total):
-            bps, fps, t, n_s, desc = oracle_sample(items, per_step)
+            cb = cpu_baseline(head, items, per_step, unit_of(head))
+            desc = cb["sample"]
             if k >= args.warmup:
-                vals.append(bps)
-        ncores = oracle.num_threads()
-        v = statistics.mean(vals) / 1e9
-        line = {"metric": METRIC, "value": round(v, 3), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+                vals.append(cb["value"])
+        v = statistics.mean(vals)
+        line = {"metric": METRIC, "value": round(v, 5), "unit": unit_of(head), "n_gpus": 1, "steps": args.steps,
                 "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f64", "data": "synthetic (SplitMix64 + Box-Muller, seed 0)", "impl": "reference",
-                "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload},
-                "cpu_baseline": {"value": round(v, 3), "unit": "GB/s", "cores": ncores, "kind": "oracle",
-                                 "sample": desc},
-                "e2e": {"value": round(v, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+                "config": {"workload": WORKLOAD_TEXT[head], "name": head},
+                "cpu_baseline": {"value": round(v, 5), "unit": unit_of(head), "cores": cb["cores"],
+                                 "cpu_model": cb["cpu_model"], "kind": "oracle", "sample": desc},
+                "e2e": {"value": round(v, 5), "unit": unit_of(head), "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
 
@@ -564,14 +730,38 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group("nccl")
-    out, items = gpu_arm(args, rank, world)
+    recs, items_of, fma_tflops, peaks = gpu_arm(args, names, rank, world)
     if rank == 0:
+        head = head if head in recs else next(iter(recs))
         if not args.no_cpu_baseline:
-            import oracle
-            bps, fps, t, n_s, desc = oracle_sample(items, args.cpu_seconds)
-            out["cpu_baseline"] = {"value": round(bps / 1e9, 3), "unit": "GB/s", "cores": oracle.num_threads(),
-                                   "kind": "oracle", "sample": desc, "seconds": round(t, 2),
-                                   "tflops_valid": round(2 * fps / 1e12, 5)}
+            for n in recs:
+                recs[n]["cpu_baseline"] = cpu_baseline(n, items_of[n], args.cpu_seconds, recs[n]["unit"])
+        h = recs[head]
+        head_clocks = clock_summary(h["clock_lines"])
+        lines = [ln for r in recs.values() for ln in r.pop("clock_lines")]
+        out = {
+            "metric": METRIC, "value": h["value"], "unit": h["unit"], "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": h["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": h["dtype"],
+            "data": "synthetic (SplitMix64 + Box-Muller, seed 0)",
+            "config": {"workload": h["workload"], "name": head,
+                       **({"layers": args.layers} if args.layers else {}),
+                       **({"batch_override": args.batch} if args.batch else {}),
+                       "parallelism": f"replicas x{world} (no collective)",
+                       "l2": "flushed before every call (2x L2 written, then a clean 2x L2 buffer read: inputs "
+                             "not cached, no dirty lines left); inputs resident in HBM",
+                       "step_bytes": h["step_bytes"], "step_fma_valid": h["step_fma_valid"],
+                       "GBps": h["GBps"], "tflops_valid": h["TFLOPs_valid"]},
+            "roofline": h["roofline"],
+            "e2e": h["e2e"],
+            "gpu_launches": h["gpu_launches"],
+            "gpu_launches_all_workloads": sum(r["gpu_launches"] for r in recs.values()),
+            "clocks": head_clocks or clock_summary(lines),
+            "clocks_all_workloads": clock_summary(lines),
+            "fp32_fma_probe_tflops": round(fma_tflops, 2),
+            **({"cpu_baseline": h["cpu_baseline"]} if "cpu_baseline" in h else {}),
+            "configs": recs,
+        }
         print(json.dumps(out))
     if world > 1:
         import torch.distributed as dist

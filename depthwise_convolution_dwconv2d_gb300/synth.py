@@ -22,6 +22,8 @@ w = 1 + 16 i and bias = 2 + 16 i.
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 
 GAMMA = np.uint64(0x9E3779B97F4A7C15)
@@ -54,12 +56,31 @@ def raw_u64(seed: int, stream: int, start: int, count: int) -> np.ndarray:
         return _mix64(base + k * GAMMA)
 
 
+def _parallel(count: int, step: int, fill) -> None:
+    """Run ``fill(start, n)`` over [0, count) in pieces of ``step``. Large
+    tensors are filled by a few threads at once (numpy releases the GIL on
+    these array operations); the values do not depend on the split, because
+    every element is a function of its own counter."""
+    pieces = [(s, min(step, count - s)) for s in range(0, count, step)]
+    if len(pieces) <= 2:
+        for s, n in pieces:
+            fill(s, n)
+        return
+    from concurrent.futures import ThreadPoolExecutor
+    workers = max(1, min(len(pieces), (os.cpu_count() or 2), 16))
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        for f in [ex.submit(fill, s, n) for s, n in pieces]:
+            f.result()
+
+
 def uniform(seed: int, stream: int, count: int) -> np.ndarray:
     """``count`` float64 uniforms on [0, 1)."""
     out = np.empty(count, dtype=np.float64)
-    for s in range(0, count, _CHUNK):
-        n = min(_CHUNK, count - s)
+
+    def fill(s, n):
         out[s:s + n] = (raw_u64(seed, stream, s, n) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+
+    _parallel(count, _CHUNK, fill)
     return out
 
 
@@ -67,9 +88,8 @@ def normal(seed: int, stream: int, count: int) -> np.ndarray:
     """``count`` float64 standard normals (Box-Muller on uniform pairs)."""
     out = np.empty(count, dtype=np.float64)
     pairs = (count + 1) // 2
-    step = _CHUNK // 2
-    for p0 in range(0, pairs, step):
-        np_ = min(step, pairs - p0)
+
+    def fill(p0, np_):
         u = (raw_u64(seed, stream, 2 * p0, 2 * np_) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
         u1, u2 = u[0::2], u[1::2]
         r = np.sqrt(-2.0 * np.log1p(-u1))
@@ -79,6 +99,8 @@ def normal(seed: int, stream: int, count: int) -> np.ndarray:
         z[1::2] = r * np.sin(t)
         n = min(2 * np_, count - 2 * p0)
         out[2 * p0:2 * p0 + n] = z[:n]
+
+    _parallel(pairs, _CHUNK // 2, fill)
     return out
 
 
@@ -105,17 +127,25 @@ class Tensor:
         v32 = values64.astype(np.float32).reshape(shape)
         self.dtype = dtype
         self.shape = tuple(shape)
+        self._f64 = None
         if dtype == "f32":
             self.store = v32
-            self.f64 = v32.astype(np.float64)
         elif dtype == "f16":
             self.store = v32.astype(np.float16)
-            self.f64 = self.store.astype(np.float64)
         elif dtype == "bf16":
             self.store = round_bf16_bits(v32).reshape(shape)
-            self.f64 = bf16_bits_to_f64(self.store).reshape(shape)
         else:
             raise ValueError(f"unknown dtype {dtype!r}")
+
+    @property
+    def f64(self) -> np.ndarray:
+        """The stored values widened exactly to float64 (computed on first use)."""
+        if self._f64 is None:
+            if self.dtype == "bf16":
+                self._f64 = bf16_bits_to_f64(self.store).reshape(self.shape)
+            else:
+                self._f64 = self.store.astype(np.float64)
+        return self._f64
 
     @property
     def nbytes(self) -> int:

@@ -120,17 +120,28 @@ class Inputs:
     extra: dict = field(default_factory=dict)
 
 
-def make_inputs(L: Layer, seed: int = 0, branch: int = 0, gy_channels: int | None = None) -> Inputs:
-    """x, w, bias and grad_out for one layer, drawn as the module docstring says."""
+def make_x(L: Layer, seed: int = 0) -> synth.Tensor:
     xs = (L.N, L.C, L.H, L.W)
     if L.x_dist == "uniform":
-        x = synth.uniform_tensor(xs, L.dtype, seed, synth.STREAM_X)
-    else:
-        x = synth.normal_tensor(xs, L.dtype, seed, synth.STREAM_X)
+        return synth.uniform_tensor(xs, L.dtype, seed, synth.STREAM_X)
+    return synth.normal_tensor(xs, L.dtype, seed, synth.STREAM_X)
+
+
+def make_w(L: Layer, seed: int = 0, branch: int = 0) -> synth.Tensor:
     w_std = L.w_std if L.w_std is not None else 1.0 / L.k
-    w = synth.normal_tensor((L.OC, L.k, L.k), L.dtype, seed, synth.STREAM_W + 16 * branch, std=w_std)
-    b = (synth.normal_tensor((L.OC,), L.dtype, seed, synth.STREAM_B + 16 * branch, std=L.b_std)
-         if L.bias else None)
+    return synth.normal_tensor((L.OC, L.k, L.k), L.dtype, seed, synth.STREAM_W + 16 * branch, std=w_std)
+
+
+def make_b(L: Layer, seed: int = 0, branch: int = 0) -> synth.Tensor:
+    return synth.normal_tensor((L.OC,), L.dtype, seed, synth.STREAM_B + 16 * branch, std=L.b_std)
+
+
+def make_gy(L: Layer, seed: int = 0, gy_channels: int | None = None) -> synth.Tensor:
     gc = L.OC if gy_channels is None else gy_channels
-    gy = synth.normal_tensor((L.N, gc, L.Ho, L.Wo), L.dtype, seed, synth.STREAM_GY)
-    return Inputs(x, w, b, gy)
+    return synth.normal_tensor((L.N, gc, L.Ho, L.Wo), L.dtype, seed, synth.STREAM_GY)
+
+
+def make_inputs(L: Layer, seed: int = 0, branch: int = 0, gy_channels: int | None = None) -> Inputs:
+    """x, w, bias and grad_out for one layer, drawn as the module docstring says."""
+    return Inputs(make_x(L, seed), make_w(L, seed, branch), make_b(L, seed, branch) if L.bias else None,
+                  make_gy(L, seed, gy_channels))
