@@ -1,0 +1,10 @@
+// Large-kernel family for 29 x 29 filters: forward, stride-1 grad-input and
+// weight gradient (kernels in large_impl.cuh).
+#include "large_entries.h"
+#include "large_impl.cuh"
+
+namespace dwconv {
+namespace large {
+DW_LARGE_DEFINE(29)
+}  // namespace large
+}  // namespace dwconv

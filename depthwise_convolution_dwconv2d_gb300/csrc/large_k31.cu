@@ -1,0 +1,10 @@
+// Large-kernel family for 31 x 31 filters: forward, stride-1 grad-input and
+// weight gradient (kernels in large_impl.cuh).
+#include "large_entries.h"
+#include "large_impl.cuh"
+
+namespace dwconv {
+namespace large {
+DW_LARGE_DEFINE(31)
+}  // namespace large
+}  // namespace dwconv

@@ -25,23 +25,27 @@ constexpr size_t kScratchBytes = size_t(8) << 20;  // 8 MiB of fp32 partial sums
 __device__ __align__(256) float g_scratch[kScratchBytes / sizeof(float)];
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_once[kMaxDevices];
+std::mutex g_mu;
+bool g_found[kMaxDevices];
 void* g_addr[kMaxDevices];
-cudaError_t g_err[kMaxDevices];
 
-// Device address of g_scratch on the current device (looked up on the first
-// call made with that device current, then reused).
+// Device address of g_scratch on the current device. Only a successful
+// lookup is kept: a lookup that fails (for example one attempted while a
+// stream is being captured, or with an earlier error still pending) is
+// retried on the next call instead of poisoning the device for good.
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::call_once(g_once[dev], [dev] {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_found[dev]) {
     void* p = nullptr;
-    g_err[dev] = cudaGetSymbolAddress(&p, g_scratch);
+    e = cudaGetSymbolAddress(&p, g_scratch);
+    if (e != cudaSuccess) return e;
     g_addr[dev] = p;
-  });
-  if (g_err[dev] != cudaSuccess) return g_err[dev];
+    g_found[dev] = true;
+  }
   *out = g_addr[dev];
   return cudaSuccess;
 }

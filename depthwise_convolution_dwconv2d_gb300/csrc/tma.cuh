@@ -75,13 +75,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for phase `parity` of `bar`; false (and *timeouts
-// incremented once per CTA) if it did not complete.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* timeouts) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
+// Bounded wait for phase `parity` of `bar` (at most `limit` polls); false
+// (and *timeouts incremented once per CTA) if it did not complete.
+__device__ __forceinline__ bool mbar_wait_n(uint64_t* bar, uint32_t parity, unsigned int* timeouts,
+                                            uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   if (threadIdx.x == 0 && timeouts) atomicAdd(timeouts, 1u);
   return false;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* timeouts) {
+  return mbar_wait_n(bar, parity, timeouts, kWaitLimit);
 }
 
 // Host: encode a 3-D tiled tensor map over a row-major [planes][rows][cols]

@@ -44,9 +44,14 @@
  *    (DWCONV_ERR_MISALIGNED otherwise); wider alignment is used when present.
  *  - Determinism: every entry point gives bitwise identical results on
  *    repeated calls with the same inputs on the same GPU.
- *  - Thread safety: no mutable global state (apart from the per-device
- *    address that dwconv2d_bwd_weight_noalloc caches); calls may come from
- *    any thread.
+ *  - Thread safety: calls may come from any thread. The library keeps
+ *    three pieces of global state: the device counter of bounded waits that
+ *    gave up (dwconv_device_timeouts), the per-device address cache of
+ *    dwconv2d_bwd_weight_noalloc (guarded by a mutex), and that entry
+ *    point's fixed scratch array, which all its calls share: calls of
+ *    dwconv2d_bwd_weight_noalloc that can overlap on the GPU must be
+ *    serialised by the caller. Every other entry point touches only the
+ *    memory its arguments name.
  *  - Empty batch (N == 0) is valid and enqueues nothing.
  */
 #ifndef DWCONV_H_
@@ -138,7 +143,8 @@ dwconv_status_t dwconv2d_bwd_weight(const dwconv2d_desc_t* desc, const void* x, 
  * dwconv2d_bwd_weight_workspace_size exceeds 8 MiB are rejected with
  * DWCONV_ERR_WORKSPACE and nothing is enqueued. The call allocates and frees
  * nothing. The first call on each device (with that device current) looks up
- * the array's device address and keeps it for later calls; make that first
+ * the array's device address and keeps it for later calls (a failed lookup
+ * returns DWCONV_ERR_CUDA and is retried by the next call); make that first
  * call before any stream capture. All calls share the one array and each
  * call's first pass overwrites every slot its second pass reads, so stale
  * contents from an earlier call do no harm -- but calls that may run at the
@@ -194,6 +200,16 @@ const char* dwconv2d_multi_plan_name(int nbranch, const dwconv2d_desc_t* descs);
  * the kernel stops early instead of hanging, leaving its outputs incomplete.
  * Synchronous: copies the counter to *count. */
 dwconv_status_t dwconv_device_timeouts(unsigned int* count);
+
+/* Health-check helper, not part of the convolution: exercises the give-up
+ * path of the library's bounded waits. One CTA waits, at most `polls`
+ * (1..65536) polls, on a shared-memory barrier that nothing will ever
+ * complete -- no copy or tensor-core operation targets it, so nothing is in
+ * flight -- gives up, adds one to the counter that dwconv_device_timeouts
+ * reads, and returns. After the kernel has run, that counter is larger by
+ * exactly one. Asynchronous like the other entry points;
+ * DWCONV_ERR_INVALID_ARG for `polls` out of range. */
+dwconv_status_t dwconv_wait_selftest(unsigned int polls, cudaStream_t stream);
 
 /* Measurement helper, not part of the convolution: runs a register-only
  * fp32 FMA loop on every SM (`blocks` x 256 threads, `iters` iterations of 16

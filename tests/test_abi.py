@@ -198,11 +198,28 @@ def test_tile_routing_respects_band_limits(lib):
 def test_large_weight_gradient_routing_respects_shared_memory(lib):
     """The large-filter weight gradient stages two fp32 (x tile + grad_out
     plane) stages; from 112 x 112 planes it would need more than its 220 KB
-    limit (k = 9 at 112 x 112: 2 x 27,904 floats + 28 group sums of 82 floats
-    + 8 = 232 KB), so those shapes take the generic weight gradient while the
+    limit (k = 9 at 112 x 112: 2 x (123 rows x 132 + 112 x 112) floats =
+    230 KB), so those shapes take the generic weight gradient while the
     forward and grad-input stay on the large kernels."""
     big = B.make_desc(4, 8, 112, 112, 9, 1, 4)
     assert B.dwconv2d_plan_name(big, 0) == "large"
     assert B.dwconv2d_plan_name(big, 2) == "generic"
     fits = B.make_desc(4, 8, 96, 96, 31, 1, 15)
     assert B.dwconv2d_plan_name(fits, 2) == "large"
+
+
+def test_every_odd_large_filter_has_a_specialised_plan(lib):
+    """Every odd filter size from 7 to 31 at the large-kernel sweep's sizes
+    (64 x 384 x {32, 48, 64}^2, stride 1, pad k // 2) plans to a specialised
+    family for all three passes: the direct large kernels for fp32 (the tile
+    kernels for 7), the tensor-core kernel for the fp16 forward and
+    grad-input from 9 up."""
+    for k in range(7, 32, 2):
+        for h in (32, 48, 64):
+            d32 = B.make_desc(64, 384, h, h, k, 1, k // 2, 1, 1, "f32")
+            d16 = B.make_desc(64, 384, h, h, k, 1, k // 2, 1, 1, "f16")
+            want = "tile" if k == 7 else "large"
+            assert [B.dwconv2d_plan_name(d32, p) for p in range(3)] == [want] * 3, (k, h)
+            p16 = [B.dwconv2d_plan_name(d16, p) for p in range(3)]
+            assert p16[:2] == (["tile"] * 2 if k == 7 else ["ibgemm"] * 2), (k, h, p16)
+            assert p16[2] == want, (k, h, p16)

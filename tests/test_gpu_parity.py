@@ -129,7 +129,9 @@ def _largek_inputs(L):
 
 @pytest.mark.parametrize("L", WL.largek(), ids=lambda L: L.name)
 def test_largek_full_size_sampled(L):
-    check_sampled(L, _largek_inputs(L), [0, 63], [0, 383], L.name)
+    # edge and interior samples and channels: the persistent kernels' units
+    # straddle plane groups, so the middle of the tensor is checked too
+    check_sampled(L, _largek_inputs(L), [0, 31, 63], [0, 1, 191, 383], L.name)
 
 
 def run_multi(M, xs, wsx, gy_t):
@@ -342,6 +344,51 @@ def test_large_kernels_planes_straddle_samples(L):
     """Large kernels where a CTA's planes span two samples (C not a multiple
     of the planes per CTA), with bias and non-"same" padding."""
     check_full(L, WL.make_inputs(L), L.label())
+
+
+def _large_direct_cases():
+    """Every odd filter size 9..31 on the direct large kernels: ragged planes
+    (widths that are not multiples of the 8-column blocks), planes above and
+    below 32 rows (two- and four-row blocks), "same" and other paddings,
+    every storage type, bias on some."""
+    cases = []
+    for i, k in enumerate(range(9, 32, 2)):
+        H = [12, 37, 20, 45, 33, 19][i % 6] + (k if i % 2 else 0) // 3
+        W = [16, 13, 41, 24, 35, 9][(i + 1) % 6] + k // 4
+        p = k // 2 if i % 3 else max(0, k // 2 - 3)
+        dt = ["f32", "f16", "bf16"][i % 3]
+        cases.append(WL.Layer(N=2 + i % 2, C=3 + i % 3, H=H, W=W, k=k, p=p, bias=i % 2 == 1, dtype=dt,
+                              name=f"k{k}H{H}W{W}p{p}{dt}"))
+    return cases
+
+
+@pytest.mark.parametrize("L", _large_direct_cases(), ids=lambda L: L.name)
+def test_large_direct_every_odd_filter(L):
+    """The direct large kernels (16-bit forward and grad-input kept off the
+    tensor cores) against the oracle, including the 17/19/23/25/29 sizes."""
+    os.environ["DWCONV_FORCE_ALGO"] = "direct"
+    try:
+        d = desc_of(L)
+        assert [B.dwconv2d_plan_name(d, q) for q in range(3)] == ["large"] * 3
+        check_full(L, WL.make_inputs(L), L.label())
+    finally:
+        del os.environ["DWCONV_FORCE_ALGO"]
+
+
+def test_large_direct_accumulate_into_gx():
+    """The stride-1 grad-input of the direct large kernels adds into gx when
+    asked (accumulate = 1)."""
+    th = torch()
+    L = WL.Layer(N=2, C=3, H=40, W=21, k=17, p=8, dtype="f32")
+    inp = WL.make_inputs(L)
+    d = desc_of(L)
+    gy, w = to_dev(inp.gy), to_dev(inp.w)
+    base = synth.normal_tensor((L.N, L.C, L.H, L.W), "f32", 5, 0)
+    gx = to_dev(base)
+    B.dwconv2d_bwd_data(d, gy, w, gx, 1)
+    th.cuda.synchronize()
+    ref = base.f64 + oracle.bwd_data(oconv(L), inp.gy.f64, inp.w.f64)
+    assert_close(to_f64(gx), ref, "f32", L.k * L.k, "accumulated gx")
 
 
 # ------------------------------------------------ tensor-core large kernels

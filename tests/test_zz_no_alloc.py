@@ -2,17 +2,20 @@
 
 It serves callers that cannot allocate device memory when they need the
 gradient (a host application that owns all device allocations, or a loop
-that cannot afford a cudaMalloc). It must give the same gradients as
-dwconv2d_bwd_weight with a caller-provided workspace, on consecutive calls
-that share its fixed device array. This file is collected last so that a
-run stopping at the first failure has already run every other test.
+that cannot afford a cudaMalloc). It runs the same kernels as
+dwconv2d_bwd_weight with a caller-provided workspace, so on consecutive
+calls that share its fixed device array its gradients must equal that entry
+point's bit for bit, and match the fp64 oracle within the parity tolerance.
+This file is collected last so that a run stopping at the first failure has
+already run every other test.
 """
 import numpy as np
 import pytest
 
+import oracle
 from depthwise_convolution_dwconv2d_gb300 import binding as B
 from depthwise_convolution_dwconv2d_gb300 import workloads as WL
-from dw_testutil import assert_close, empty_dev, to_dev, to_f64, torch, ws_for
+from dw_testutil import assert_close, empty_dev, oconv, to_dev, to_f64, torch, ws_for
 
 pytestmark = pytest.mark.gpu
 
@@ -49,18 +52,25 @@ CALLS = [WL.Layer(N=8, C=64, H=56, W=56, k=3, s=1, p=1, name="mb56"),
                   x_dist="normal", w_std=0.2, name="mult_bf16")]
 
 
+def check_against_workspace_call_and_oracle(L, label):
+    ref_w, ref_b = grads(L, use_noalloc=False)
+    got_w, got_b = grads(L, use_noalloc=True)
+    # the same kernels and the same summation order: bitwise equal
+    assert np.array_equal(got_w, ref_w), f"{label} gw differs from the workspace entry point"
+    if L.bias:
+        assert np.array_equal(got_b, ref_b), f"{label} gb differs from the workspace entry point"
+    inp = WL.make_inputs(L)
+    rgw, rgb = oracle.bwd_weight(oconv(L), inp.x.f64, inp.gy.f64, want_w=True, want_b=L.bias)
+    assert_close(got_w, rgw, L.dtype, L.k * L.k, f"{label} gw vs oracle")
+    if L.bias:
+        assert_close(got_b, rgb, L.dtype, 1, f"{label} gb vs oracle")
+
+
 def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
     for L in CALLS:
-        ref_w, ref_b = grads(L, use_noalloc=False)
-        got_w, got_b = grads(L, use_noalloc=True)
-        assert_close(got_w, ref_w, L.dtype, L.k * L.k, f"{L.name} gw")
-        if L.bias:
-            assert_close(got_b, ref_b, L.dtype, 1, f"{L.name} gb")
+        check_against_workspace_call_and_oracle(L, L.name)
     # and once more on the first shape, after the second call reused the array
-    L = CALLS[0]
-    ref_w, _ = grads(L, use_noalloc=False)
-    got_w, _ = grads(L, use_noalloc=True)
-    assert_close(got_w, ref_w, L.dtype, L.k * L.k, "repeat gw")
+    check_against_workspace_call_and_oracle(CALLS[0], "repeat")
 
 
 def test_noalloc_rejects_descriptors_beyond_the_array():
