@@ -24,7 +24,7 @@ SYMBOLS = ("dwconv2d_output_shape", "dwconv2d_fwd", "dwconv2d_bwd_data",
            "dwconv2d_bwd_weight_workspace_size", "dwconv2d_bwd_weight", "dwconv2d_fwd_multi",
            "dwconv2d_bwd_data_multi", "dwconv_status_string", "dwconv2d_plan_name",
            "dwconv2d_multi_plan_name", "dwconv_fma_probe", "dwconv2d_bwd_weight_noalloc",
-           "dwconv_device_timeouts")
+           "dwconv_device_timeouts", "dwconv_wait_selftest")
 
 
 class DwconvError(RuntimeError):
@@ -97,6 +97,7 @@ def load():
     lib.dwconv2d_multi_plan_name.restype = ctypes.c_char_p
     lib.dwconv_device_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     lib.dwconv_fma_probe.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp]
+    lib.dwconv_wait_selftest.argtypes = [ctypes.c_uint, vp]
     for name in SYMBOLS:
         if name not in ("dwconv2d_bwd_weight_workspace_size", "dwconv_status_string", "dwconv2d_plan_name",
                         "dwconv2d_multi_plan_name"):
@@ -210,3 +211,7 @@ def dwconv_device_timeouts() -> int:
 
 def dwconv_fma_probe(blocks: int, iters: int, sink, stream=None):
     _check(load().dwconv_fma_probe(int(blocks), int(iters), _ptr(sink), _stream(stream)), "dwconv_fma_probe")
+
+
+def dwconv_wait_selftest(polls: int, stream=None):
+    _check(load().dwconv_wait_selftest(int(polls), _stream(stream)), "dwconv_wait_selftest")
