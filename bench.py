@@ -70,6 +70,7 @@ FAMILY_SOURCES = {
     "plane": ("common.cuh", "plan.h", "plane.cu", "generic.cu"),
     "large": ("common.cuh", "plan.h", "tile.cuh", "large.cu", "large_impl.cuh", "generic.cu"),
     "ibgemm": ("common.cuh", "plan.h", "tma.cuh", "tma.cu", "ibgemm.cu"),
+    "tcwgrad": ("common.cuh", "plan.h", "tma.cuh", "tma.cu", "wgrad_tc.cu", "generic.cu"),
     "generic": ("common.cuh", "plan.h", "generic.cu"),
 }
 
@@ -601,7 +602,7 @@ def time_workload(name, items, args, dev, stream, world, dist, peaks, fma_tflops
     for key, f in fams.items():
         pass_, plan, dt = key.split(":")
         family = plan.replace("multi-", "")
-        if family == "ibgemm":
+        if family in ("ibgemm", "tcwgrad"):
             bp = ("tensor", tc_peak, tc_src)
         elif fma_tflops:
             bp = ("alu", fma_tflops, fma_src)

@@ -31,6 +31,7 @@ const char* algo_name(Algo a) {
     case Algo::Large: return "large";
     case Algo::IBGemm: return "ibgemm";
     case Algo::Plane: return "plane";
+    case Algo::TcWgrad: return "tcwgrad";
   }
   return "unknown";
 }
@@ -56,6 +57,7 @@ Algo plan_bwd_data(const Conv& c) {
 WPlan plan_bwd_weight(const Conv& c) {
   if (!force_generic() && plane::wgrad_supported(c)) return WPlan{Algo::Plane, plane::wgrad_chunks(c)};
   if (!force_generic() && tile::wgrad_supported(c)) return WPlan{Algo::Tile, tile::wgrad_chunks(c)};
+  if (!force_generic() && allow_ibgemm() && wtc::supported(c)) return WPlan{Algo::TcWgrad, large::wgrad_chunks(c)};
   if (!force_generic() && large::wgrad_supported(c)) return WPlan{Algo::Large, large::wgrad_chunks(c)};
   // generic first pass: a chunk of whole samples per block, at most 2^20
   // positions per chunk so each thread's serial chain stays <= 4096 terms.
@@ -113,6 +115,14 @@ cudaError_t run_bwd_weight(const WPlan& p, const Conv& c, const void* x, const v
       break;
     case Algo::Large:
       e = large::wgrad(c, x, gy, ws, p.chunks, s);
+      break;
+    case Algo::TcWgrad:
+      // a misaligned pointer rules the tensor-core kernel out for this call
+      // only; the direct kernels take the same chunks (same workspace)
+      e = wtc::wgrad(c, x, gy, ws, p.chunks, s);
+      if (e == cudaErrorNotSupported)
+        e = large::wgrad_supported(c) ? large::wgrad(c, x, gy, ws, p.chunks, s)
+                                      : bwd_weight_generic_pass1(c, x, gy, ws, p.chunks, gw != nullptr, gb != nullptr, s);
       break;
     default:
       e = bwd_weight_generic_pass1(c, x, gy, ws, p.chunks, gw != nullptr, gb != nullptr, s);

@@ -13,6 +13,7 @@ enum class Algo {
   Large = 2,     // large.cu: large-kernel direct convolution
   IBGemm = 3,    // ibgemm.cu: large-kernel implicit batched GEMM on tcgen05 (fp16 / bf16)
   Plane = 4,     // plane.cu: 3x3 on small planes, one warp per group of whole planes
+  TcWgrad = 5,   // wgrad_tc.cu: large-kernel weight gradient on tcgen05 (fp16 / bf16)
 };
 
 struct WPlan {
@@ -91,5 +92,13 @@ bool bwd_data_supported(const Conv& c);
 cudaError_t fwd(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s);
 cudaError_t bwd_data(const Conv& c, const void* gy, const void* w, void* gx, bool acc, cudaStream_t s);
 }  // namespace ibg
+
+namespace wtc {
+// wgrad_tc.cu: large-kernel weight gradient (first pass) on the tensor cores,
+// 16-bit data, stride 1; cudaErrorNotSupported when this call's x or grad_out
+// pointer is not 16-byte aligned or the driver refuses its tensor maps
+bool supported(const Conv& c);
+cudaError_t wgrad(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s);
+}  // namespace wtc
 
 }  // namespace dwconv

@@ -105,6 +105,11 @@ bool encode_4d(CUtensorMap* map, const void* base, int dtype, uint64_t cols, uin
 bool encode_3d_sw128(CUtensorMap* map, const void* base, int dtype, uint64_t cols, uint64_t rows,
                      uint64_t planes, uint32_t box_cols, uint32_t box_rows, uint32_t box_planes);
 
+// Host: tiled tensor map of any rank (1..5) with explicit dimensions, byte
+// strides of dimensions 1.. (multiples of 16, in any order) and box.
+bool encode_strided(CUtensorMap* map, const void* base, int dtype, int rank, const uint64_t* dims,
+                    const uint64_t* strides, const uint32_t* box);
+
 // Host: device address of the timeout counter on the current device (looked
 // up once per device), or nullptr if the lookup failed.
 unsigned int* timeout_counter();

@@ -182,9 +182,10 @@ const char* dwconv_status_string(dwconv_status_t status);
  * planes, one warp per group of whole planes), "tile" (small filters),
  * "large" (large-filter direct convolution), "ibgemm" (large-filter fp16 /
  * bf16 forward and grad-input as an implicit batched GEMM on the tensor
+ * cores), "tcwgrad" (large-filter fp16 / bf16 weight gradient on the tensor
  * cores), "generic" (any shape) or "invalid". Host only; for logs and tests.
- * An "ibgemm" pass whose input pointer is not 16-byte aligned runs on the
- * direct kernels instead. */
+ * An "ibgemm" pass whose input pointer (a "tcwgrad" pass whose x or grad_out
+ * pointer) is not 16-byte aligned runs on the direct kernels instead. */
 const char* dwconv2d_plan_name(const dwconv2d_desc_t* desc, int pass);
 
 /* Kernel family used by dwconv2d_fwd_multi / dwconv2d_bwd_data_multi for

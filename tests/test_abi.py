@@ -212,8 +212,8 @@ def test_every_odd_large_filter_has_a_specialised_plan(lib):
     """Every odd filter size from 7 to 31 at the large-kernel sweep's sizes
     (64 x 384 x {32, 48, 64}^2, stride 1, pad k // 2) plans to a specialised
     family for all three passes: the direct large kernels for fp32 (the tile
-    kernels for 7), the tensor-core kernel for the fp16 forward and
-    grad-input from 9 up."""
+    kernels for 7), the tensor-core kernels for the fp16 forward, grad-input
+    and weight gradient from 9 up."""
     for k in range(7, 32, 2):
         for h in (32, 48, 64):
             d32 = B.make_desc(64, 384, h, h, k, 1, k // 2, 1, 1, "f32")
@@ -222,4 +222,4 @@ def test_every_odd_large_filter_has_a_specialised_plan(lib):
             assert [B.dwconv2d_plan_name(d32, p) for p in range(3)] == [want] * 3, (k, h)
             p16 = [B.dwconv2d_plan_name(d16, p) for p in range(3)]
             assert p16[:2] == (["tile"] * 2 if k == 7 else ["ibgemm"] * 2), (k, h, p16)
-            assert p16[2] == want, (k, h, p16)
+            assert p16[2] == ("tile" if k == 7 else "tcwgrad"), (k, h, p16)

@@ -452,6 +452,94 @@ def test_no_bounded_wait_gave_up_after_ibgemm():
     assert B.dwconv_device_timeouts() == 0
 
 
+TCW_CASES = [
+    WL.Layer(N=5, C=3, H=32, W=32, k=31, p=15, bias=True, dtype="f16"),
+    WL.Layer(N=7, C=5, H=24, W=16, k=9, p=4, dtype="bf16"),
+    WL.Layer(N=3, C=4, H=17, W=24, k=13, p=2, bias=True, dtype="f16"),
+    WL.Layer(N=2, C=3, H=40, W=40, k=17, p=8, dtype="bf16"),
+    WL.Layer(N=11, C=2, H=16, W=16, k=15, p=7, bias=True, dtype="bf16"),
+    WL.Layer(N=2, C=3, H=64, W=64, k=27, p=13, dtype="f16"),
+]
+TCW_IDS = ["k31f16_b", "k9bf16_W16", "k13f16_p2", "k17bf16", "k15bf16_N11", "k27f16_64"]
+
+
+@pytest.mark.parametrize("L", TCW_CASES, ids=TCW_IDS)
+def test_tensor_core_weight_gradient_vs_oracle(L):
+    """Large-filter fp16 / bf16 weight gradient on the tensor cores: "same"
+    and other paddings, planes taller than wide, batch chunks of several
+    samples, several channels, bias gradient."""
+    d = desc_of(L)
+    if L.Wo % 8 == 0:
+        assert B.dwconv2d_plan_name(d, 2) == "tcwgrad"
+    check_full(L, WL.make_inputs(L), L.label())
+
+
+def test_tensor_core_weight_gradient_reads_its_slice():
+    """The weight gradient reads grad_out from a channel slice of a wider
+    tensor (offset 3 of 11 channels)."""
+    th = torch()
+    L = WL.Layer(N=3, C=4, H=24, W=24, k=11, p=5, bias=True, dtype="f16")
+    inp = WL.make_inputs(L, gy_channels=11)
+    d = desc_of(L, off=3, c_total=11)
+    assert B.dwconv2d_plan_name(d, 2) == "tcwgrad"
+    x, gy = to_dev(inp.x), to_dev(inp.gy)
+    gw = empty_dev((L.OC, L.k, L.k), L.dtype)
+    gb = empty_dev((L.OC,), L.dtype)
+    ws, nbytes = ws_for(d)
+    B.dwconv2d_bwd_weight(d, x, gy, gw, gb, ws, nbytes)
+    th.cuda.synchronize()
+    rgw, rgb = oracle.bwd_weight(oconv(L, off=3, c_total=11), inp.x.f64, inp.gy.f64, want_w=True, want_b=True)
+    assert_close(to_f64(gw), rgw, L.dtype, L.k * L.k, "sliced gw")
+    assert_close(to_f64(gb), rgb, L.dtype, 1, "sliced gb")
+
+
+def test_tensor_core_weight_gradient_deterministic_and_matches_direct():
+    """Bitwise repeatable, and within the fp16 tolerance of the direct
+    (FMA) weight gradient."""
+    th = torch()
+    L = TCW_CASES[0]
+    inp = WL.make_inputs(L)
+    d = desc_of(L)
+    x, gy = to_dev(inp.x), to_dev(inp.gy)
+    outs = []
+    for force in (None, None, "direct"):
+        if force:
+            os.environ["DWCONV_FORCE_ALGO"] = force
+        try:
+            gw = empty_dev((L.OC, L.k, L.k), L.dtype)
+            ws, nbytes = ws_for(d)
+            B.dwconv2d_bwd_weight(d, x, gy, gw, None, ws, nbytes)
+            th.cuda.synchronize()
+            outs.append(to_f64(gw))
+        finally:
+            if force:
+                del os.environ["DWCONV_FORCE_ALGO"]
+    assert np.array_equal(outs[0], outs[1])
+    assert_close(outs[0], outs[2], L.dtype, L.k * L.k, "tensor-core vs direct gw")
+
+
+def test_tensor_core_weight_gradient_misaligned_input_falls_back():
+    """An x pointer off the 16-byte grid runs on the direct kernels."""
+    th = torch()
+    L = TCW_CASES[1]
+    inp = WL.make_inputs(L)
+    d = desc_of(L)
+    n = L.N * L.C * L.H * L.W
+    xbuf = empty_dev((n + 8,), L.dtype)
+    xv = xbuf[1:1 + n].view(L.N, L.C, L.H, L.W)
+    xv.copy_(to_dev(inp.x))
+    gw = empty_dev((L.OC, L.k, L.k), L.dtype)
+    ws, nbytes = ws_for(d)
+    B.dwconv2d_bwd_weight(d, xv, to_dev(inp.gy), gw, None, ws, nbytes)
+    th.cuda.synchronize()
+    rgw, _ = oracle.bwd_weight(oconv(L), inp.x.f64, inp.gy.f64)
+    assert_close(to_f64(gw), rgw, L.dtype, L.k * L.k, "misaligned gw")
+
+
+def test_no_bounded_wait_gave_up_after_tensor_core_wgrad():
+    assert B.dwconv_device_timeouts() == 0
+
+
 # ------------------------------------------------------ small-plane kernels
 PLANE_CASES = [
     WL.Layer(N=3, C=5, H=14, W=14, k=3, s=1, p=1, bias=True, dtype="f32"),
