@@ -391,6 +391,25 @@ def test_large_direct_accumulate_into_gx():
     assert_close(to_f64(gx), ref, "f32", L.k * L.k, "accumulated gx")
 
 
+CLIFF_CASES = [
+    WL.Layer(N=3, C=5, H=56, W=56, k=3, s=3, p=1, bias=True, dtype="f32", name="k3s3p1_f32"),
+    WL.Layer(N=2, C=4, H=29, W=31, k=3, s=3, p=0, dtype="bf16", name="k3s3p0_bf16"),
+    WL.Layer(N=3, C=5, H=40, W=36, k=5, s=1, p=6, d=3, bias=True, dtype="f32", name="k5d3_f32"),
+    WL.Layer(N=2, C=3, H=33, W=27, k=5, s=1, p=6, d=3, dtype="f16", name="k5d3_f16"),
+    WL.Layer(N=3, C=4, H=56, W=56, k=7, s=2, p=3, dtype="f32", name="k7s2_f32"),
+    WL.Layer(N=2, C=3, H=30, W=34, k=7, s=2, p=3, bias=True, dtype="bf16", name="k7s2_bf16"),
+]
+
+
+@pytest.mark.parametrize("L", CLIFF_CASES, ids=lambda L: L.name)
+def test_tile_kernels_for_stride3_dilation3_and_7x7_stride2(L):
+    """3x3 stride 3, 5x5 dilation 3 and the 7x7 stride-2 weight gradient run
+    on the tile kernels (not the generic one-output-per-thread kernels)."""
+    d = desc_of(L)
+    assert [B.dwconv2d_plan_name(d, q) for q in range(3)] == ["tile"] * 3
+    check_full(L, WL.make_inputs(L), L.label())
+
+
 # ------------------------------------------------ tensor-core large kernels
 IBG_CASES = [
     WL.Layer(N=3, C=5, H=32, W=32, k=31, p=15, bias=True, dtype="f16"),
