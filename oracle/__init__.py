@@ -6,7 +6,8 @@ package, and this package never imports the product. It shares no code with
 the CUDA library.
 
 The arithmetic lives in ``dwconv_oracle.c`` (direct nested loops over the
-definition of forward, bwd_data and bwd_weight). This module only compiles it
+definition of forward, bwd_data and bwd_weight, and the per-channel epilogue
+of the fused forward). This module only compiles it
 with gcc, marshals numpy float64 arrays to it, and expresses the fused
 multi-branch calls the way the DynamicConvolutionOperator README describes
 them ("Solution": one output per dilation branch, each stored into its own
@@ -120,6 +121,7 @@ def _load():
         lib.oracle_dwconv2d_fwd.argtypes = [P, dp, dp, dp, dp]
         lib.oracle_dwconv2d_bwd_data.argtypes = [P, dp, dp, dp]
         lib.oracle_dwconv2d_bwd_weight.argtypes = [P, dp, dp, dp, dp]
+        lib.oracle_epilogue.argtypes = [P, dp, dp, ctypes.c_int, dp]
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -152,6 +154,23 @@ def fwd(cv: Conv, x, w, bias=None, y=None):
     assert y.shape == (cv.N, cv.Ctot, cv.Ho, cv.Wo)
     d = cv._c()
     lib.oracle_dwconv2d_fwd(ctypes.byref(d), _ptr(x), _ptr(w), _ptr(b), _ptr(y))
+    return y
+
+
+ACTS = {"none": 0, "relu": 1, "relu6": 2}
+
+
+def fwd_epilogue(cv: Conv, x, w, bias=None, scale=None, shift=None, act="none", y=None):
+    """Forward, then y = act(scale[oc] * y + shift[oc]) on this op's channels.
+
+    ``act`` is "none", "relu" (max(v, 0)) or "relu6" (min(max(v, 0), 6));
+    scale / shift of None mean 1 / 0.
+    """
+    y = fwd(cv, x, w, bias, y)
+    sc = None if scale is None else _f64(scale, (cv.OC,))
+    sh = None if shift is None else _f64(shift, (cv.OC,))
+    d = cv._c()
+    _load().oracle_epilogue(ctypes.byref(d), _ptr(sc), _ptr(sh), ACTS[act], _ptr(y))
     return y
 
 

@@ -32,6 +32,8 @@
  *                                x[n, oc/m, oh*sh - ph + a*dh, ow*sw - pw + b*dw]
  *               gb[oc] = sum_{n, oh, ow} gy[n, off+oc, oh, ow]
  *               (the grad-weight kernel and grad_bias of #3057).
+ *   epilogue    y = act(scale * y + shift) per output channel after the
+ *               forward (oracle_epilogue below).
  *
  * Readings where the pages are silent: cross-correlation (no kernel flip, as
  * PyTorch's conv2d); Ho = floor((H + 2ph - dh(kh-1) - 1)/sh) + 1; symmetric
@@ -163,6 +165,33 @@ void oracle_dwconv2d_bwd_weight(const oracle_desc* d, const double* x, const dou
         for (int64_t i = 0; i < Ho * Wo; ++i) acc += gyp[i];
       }
       gb[oc] = acc;
+    }
+  }
+}
+
+/* Fused forward epilogue, applied in place to this op's channels
+ * [off, off + C*m) of y once oracle_dwconv2d_fwd has written them:
+ *   v = scale[oc] * v + shift[oc]        (scale NULL: 1, shift NULL: 0)
+ *   act 1: v = max(v, 0);  act 2: v = min(max(v, 0), 6);  act 0: unchanged.
+ * Source: the Megvii article on custom convolution operators with cutlass
+ * (its opening list: a user of a basic operator library cannot add a new
+ * activation to the convolution). Reading: scale / shift are a batch norm in
+ * inference form folded per output channel; the activation comes last. */
+void oracle_epilogue(const oracle_desc* d, const double* scale, const double* shift, int act,
+                     double* y) {
+  const int64_t Ho = oracle_out_h(d), Wo = oracle_out_w(d);
+  const int64_t OC = d->C * d->m;
+  for (int64_t n = 0; n < d->N; ++n) {
+    for (int64_t oc = 0; oc < OC; ++oc) {
+      double* yp = y + (n * d->c_total + d->off + oc) * Ho * Wo;
+      const double sc = scale ? scale[oc] : 1.0;
+      const double sh = shift ? shift[oc] : 0.0;
+      for (int64_t i = 0; i < Ho * Wo; ++i) {
+        double v = sc * yp[i] + sh;
+        if (act == 1 || act == 2) v = v > 0.0 ? v : 0.0;
+        if (act == 2) v = v < 6.0 ? v : 6.0;
+        yp[i] = v;
+      }
     }
   }
 }

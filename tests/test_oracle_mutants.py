@@ -33,6 +33,10 @@ MUTANTS = {
                                   "gw[(oc * d->kw + b) * d->kh + a] = acc;"),
     "bwd_weight_stride_dropped": ("const int64_t iw = ow * d->sw - d->pw + b * d->dw;\n                if",
                                   "const int64_t iw = ow - d->pw + b * d->dw;\n                if"),
+    "epi_shift_inside_scale": ("double v = sc * yp[i] + sh;", "double v = sc * (yp[i] + sh);"),
+    "epi_relu6_uncapped": ("if (act == 2) v = v < 6.0 ? v : 6.0;", ""),
+    "epi_scale_by_input_channel": ("const double sc = scale ? scale[oc] : 1.0;",
+                                   "const double sc = scale ? scale[oc / d->m] : 1.0;"),
     "bias_grad_short": ("for (int64_t i = 0; i < Ho * Wo; ++i) acc += gyp[i];",
                         "for (int64_t i = 1; i < Ho * Wo; ++i) acc += gyp[i];"),
 }

@@ -287,3 +287,58 @@ def test_zero_batch_and_degenerate_output():
     x = rand(1, 1, 3, 3)
     w = rand(1, 5, 5)
     assert abs(oracle.fwd(cv, x, w)[0, 0, 0, 0] - np.sum(w[0, 1:4, 1:4] * x[0, 0])) < 1e-12
+
+
+# ---- fused forward epilogue -------------------------------------------------
+
+@pytest.mark.parametrize("act", ["none", "relu", "relu6"])
+@pytest.mark.parametrize("cv", [CASES[1], CASES[40], CASES[-5]],
+                         ids=lambda c: f"k{c.kh}x{c.kw}s{c.sh}{c.sw}p{c.ph}{c.pw}d{c.dh}{c.dw}m{c.m}")
+def test_epilogue_is_batch_norm_then_activation(cv, act):
+    """A folded inference batch norm plus activation equals torch's float64
+    conv2d -> batch_norm(eval) -> relu / hardtanh(0, 6) on the same values."""
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    rng = np.random.default_rng(cv.kh * 100 + cv.sh * 10 + cv.m)
+    x, w, b = 3.0 * rng.standard_normal((cv.N, cv.C, cv.H, cv.W)), rng.standard_normal((cv.OC, cv.kh, cv.kw)), \
+        rng.standard_normal(cv.OC)
+    gamma, beta, mean = rng.standard_normal(cv.OC), rng.standard_normal(cv.OC), rng.standard_normal(cv.OC)
+    var, eps = rng.uniform(0.5, 2.0, cv.OC), 1e-5
+    scale = gamma / np.sqrt(var + eps)
+    shift = beta - mean * scale
+    ty = F.conv2d(torch.tensor(x), torch.tensor(w.reshape(cv.OC, 1, cv.kh, cv.kw)), torch.tensor(b),
+                  stride=(cv.sh, cv.sw), padding=(cv.ph, cv.pw), dilation=(cv.dh, cv.dw), groups=cv.C)
+    ty = F.batch_norm(ty, torch.tensor(mean), torch.tensor(var), torch.tensor(gamma), torch.tensor(beta),
+                      training=False, eps=eps)
+    if act == "relu":
+        ty = F.relu(ty)
+    elif act == "relu6":
+        ty = F.hardtanh(ty, 0.0, 6.0)
+    got = oracle.fwd_epilogue(cv, x, w, b, scale, shift, act)
+    np.testing.assert_allclose(got, ty.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_epilogue_identity_and_activation_cases():
+    """No scale, shift or activation is the plain forward (bit-exact); a
+    negated delta kernel with ReLU gives max(-x, 0); ReLU6 of a constant plane
+    of 7 under the same kernel and shift 13 gives 6 everywhere."""
+    cv = Conv(N=2, C=3, H=5, W=6, kh=3, kw=3, ph=1, pw=1, m=2, off=1, c_total=8)
+    x, w = rand(cv.N, cv.C, cv.H, cv.W), rand(cv.OC, 3, 3)
+    y0 = oracle.fwd(cv, x, w)
+    assert np.array_equal(oracle.fwd_epilogue(cv, x, w), y0)
+    neg = np.zeros((cv.OC, 3, 3))
+    neg[:, 1, 1] = -1.0
+    y = oracle.fwd_epilogue(cv, x, neg, act="relu")
+    want = np.maximum(-np.repeat(x, cv.m, axis=1), 0.0)
+    assert np.array_equal(y[:, 1:1 + cv.OC], want)
+    assert not y[:, 0].any() and not y[:, 1 + cv.OC:].any()
+    y6 = oracle.fwd_epilogue(cv, np.full(x.shape, 7.0), neg, shift=np.full(cv.OC, 13.0), act="relu6")
+    assert np.array_equal(y6[:, 1:1 + cv.OC], np.full((cv.N, cv.OC, cv.H, cv.W), 6.0))
+    # ReLU6 of a ramp through the identity kernel: clipped below and above
+    ramp = np.linspace(-4.0, 10.0, cv.N * cv.C * cv.H * cv.W).reshape(x.shape)
+    yr = oracle.fwd_epilogue(cv, ramp, -neg, act="relu6")
+    assert np.array_equal(yr[:, 1:1 + cv.OC], np.clip(np.repeat(ramp, cv.m, axis=1), 0.0, 6.0))
+    # scale only: channel oc multiplied by scale[oc], exactly for powers of two
+    sc = 2.0 ** np.arange(cv.OC)
+    ys = oracle.fwd_epilogue(cv, x, w, scale=sc)
+    assert np.array_equal(ys[:, 1:1 + cv.OC], y0[:, 1:1 + cv.OC] * sc[None, :, None, None])
