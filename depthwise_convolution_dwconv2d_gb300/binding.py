@@ -24,7 +24,10 @@ SYMBOLS = ("dwconv2d_output_shape", "dwconv2d_fwd", "dwconv2d_bwd_data",
            "dwconv2d_bwd_weight_workspace_size", "dwconv2d_bwd_weight", "dwconv2d_fwd_multi",
            "dwconv2d_bwd_data_multi", "dwconv_status_string", "dwconv2d_plan_name",
            "dwconv2d_multi_plan_name", "dwconv_fma_probe", "dwconv2d_bwd_weight_noalloc",
-           "dwconv_device_timeouts", "dwconv_wait_selftest")
+           "dwconv_device_timeouts", "dwconv_wait_selftest", "dwconv2d_fwd_epilogue")
+
+# dwconv_act_t
+ACTS = {"none": 0, "relu": 1, "relu6": 2}
 
 
 class DwconvError(RuntimeError):
@@ -82,6 +85,7 @@ def load():
     vp, st = ctypes.c_void_p, ctypes.c_int
     lib.dwconv2d_output_shape.argtypes = [P, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]
     lib.dwconv2d_fwd.argtypes = [P, vp, vp, vp, vp, vp]
+    lib.dwconv2d_fwd_epilogue.argtypes = [P, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp]
     lib.dwconv2d_bwd_data.argtypes = [P, vp, vp, vp, ctypes.c_int, vp]
     lib.dwconv2d_bwd_weight_workspace_size.argtypes = [P]
     lib.dwconv2d_bwd_weight_workspace_size.restype = ctypes.c_size_t
@@ -142,6 +146,14 @@ def dwconv2d_output_shape(desc: Desc):
 def dwconv2d_fwd(desc: Desc, x, w, bias, y, stream=None):
     _check(load().dwconv2d_fwd(ctypes.byref(desc), _ptr(x), _ptr(w), _ptr(bias), _ptr(y),
                                _stream(stream)), "dwconv2d_fwd")
+
+
+def dwconv2d_fwd_epilogue(desc: Desc, x, w, bias, scale, shift, act, y, stream=None):
+    """``act`` is a dwconv_act_t value or one of ``ACTS``' names."""
+    a = ACTS[act] if isinstance(act, str) else int(act)
+    _check(load().dwconv2d_fwd_epilogue(ctypes.byref(desc), _ptr(x), _ptr(w), _ptr(bias), _ptr(scale),
+                                         _ptr(shift), a, _ptr(y), _stream(stream)),
+           "dwconv2d_fwd_epilogue")
 
 
 def dwconv2d_bwd_data(desc: Desc, gy, w, gx, accumulate=0, stream=None):

@@ -92,6 +92,23 @@ template <typename T> __device__ __forceinline__ float ld_rw(const T* p) { retur
 
 
 
+// Fused epilogue of the forward: y = act(scale[oc] * (conv + bias[oc]) +
+// shift[oc]) -- a folded batch norm (scale = gamma / sqrt(var + eps), shift =
+// beta - mean * scale) and an activation, applied to the fp32 result before
+// its one rounding to the storage type. scale / shift may be null (1 / 0).
+struct Epi {
+  const void* scale;
+  const void* shift;
+  int act;  // DWCONV_ACT_*
+  __host__ __device__ bool active() const { return scale != nullptr || shift != nullptr || act != 0; }
+};
+
+__device__ __forceinline__ float epi_act(float v, int act) {
+  if (act == DWCONV_ACT_RELU) return fmaxf(v, 0.f);
+  if (act == DWCONV_ACT_RELU6) return fminf(fmaxf(v, 0.f), 6.f);
+  return v;
+}
+
 inline int div_up(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
 // Launch helpers: each family exposes launch functions templated on nothing;
@@ -107,7 +124,7 @@ inline int div_up(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / 
 // ---- kernel families (each returns cudaGetLastError() after its launches) --
 // generic.cu: correct for every valid descriptor, one output per thread.
 cudaError_t fwd_generic(const Conv& c, const void* x, const void* w, const void* b, void* y,
-                        cudaStream_t s);
+                        cudaStream_t s, const Epi& ep = Epi{});
 cudaError_t bwd_data_generic(const Conv& c, const void* gy, const void* w, void* gx,
                              bool accumulate, cudaStream_t s);
 struct MultiGeneric {

@@ -19,7 +19,7 @@ constexpr int kThreads = 256;
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 fwd_generic_kernel(Conv c, const T* __restrict__ x, const T* __restrict__ w,
-                   const T* __restrict__ b, T* __restrict__ y) {
+                   const T* __restrict__ b, T* __restrict__ y, Epi ep) {
   const int64_t total = c.N * c.OC() * c.Ho * c.Wo;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
@@ -41,6 +41,11 @@ fwd_generic_kernel(Conv c, const T* __restrict__ x, const T* __restrict__ w,
       }
     }
     if (b) acc += ld(b + oc);
+    if (ep.active()) {
+      const float sc = ep.scale ? ld(reinterpret_cast<const T*>(ep.scale) + oc) : 1.f;
+      const float sh = ep.shift ? ld(reinterpret_cast<const T*>(ep.shift) + oc) : 0.f;
+      acc = epi_act(fmaf(acc, sc, sh), ep.act);
+    }
     y[c.y_base(n, oc) + oh * c.Wo + ow] = from_f<T>(acc);
   }
 }
@@ -211,10 +216,10 @@ int grid_for(int64_t total) {
 }  // namespace
 
 cudaError_t fwd_generic(const Conv& c, const void* x, const void* w, const void* b, void* y,
-                        cudaStream_t s) {
+                        cudaStream_t s, const Epi& ep) {
   const int g = grid_for(c.N * c.OC() * c.Ho * c.Wo);
   DWCONV_DISPATCH_DTYPE(c.dtype, T,
-    fwd_generic_kernel<T><<<g, kThreads, 0, s>>>(c, (const T*)x, (const T*)w, (const T*)b, (T*)y));
+    fwd_generic_kernel<T><<<g, kThreads, 0, s>>>(c, (const T*)x, (const T*)w, (const T*)b, (T*)y, ep));
   return cudaGetLastError();
 }
 

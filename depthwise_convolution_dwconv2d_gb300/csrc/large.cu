@@ -28,9 +28,10 @@ bool wgrad_supported(const Conv& c) {
   return false;
 }
 
-cudaError_t fwd(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s) {
+cudaError_t fwd(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s,
+                const Epi& ep) {
 #define X(K) \
-  if (c.kh == K) return fwd_k##K(c, x, w, b, y, s);
+  if (c.kh == K) return fwd_k##K(c, x, w, b, y, s, ep);
   DW_LARGE_SIZES(X)
 #undef X
   return cudaErrorInvalidConfiguration;

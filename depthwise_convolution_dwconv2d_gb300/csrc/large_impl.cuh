@@ -120,7 +120,7 @@ struct LCfg {
 template <int K, int R>
 __global__ void __launch_bounds__(kNT, 2)
 dconv_kernel(Conv c, LCfg g, const void* __restrict__ in, const void* __restrict__ w,
-             const void* __restrict__ bias, void* out) {
+             const void* __restrict__ bias, void* out, Epi ep) {
   extern __shared__ __align__(16) float sm[];
   constexpr int KP = (K + 3) / 4 * 4;          // filter row stride (16-byte rows)
   constexpr int NCH = (kV + K - 1 + 3) / 4;    // window chunks per input row
@@ -228,6 +228,14 @@ dconv_kernel(Conv c, LCfg g, const void* __restrict__ in, const void* __restrict
             }
           }
         }
+      }
+      if (ep.active()) {
+        const float sc = ep.scale ? ld_any(ep.scale, ch_, g.dtype) : 1.f;
+        const float sh = ep.shift ? ld_any(ep.shift, ch_, g.dtype) : 0.f;
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int v = 0; v < kV; ++v) acc[r][v] = epi_act(fmaf(acc[r][v], sc, sh), ep.act);
       }
       const int64_t ob = g.flip ? c.x_base(n_, ch_) : c.y_base(n_, ch_);
 #pragma unroll
@@ -627,7 +635,7 @@ bool plan_dconv(const Conv& c, bool flip, LCfg* out_cfg, int* threads) {
 
 template <int K, int R>
 cudaError_t launch_dconv(const Conv& c, const LCfg& g0, int threads, const void* in, const void* w,
-                         const void* bias, void* out, bool acc, cudaStream_t s) {
+                         const void* bias, void* out, bool acc, cudaStream_t s, const Epi& ep) {
   LCfg g = g0;
   g.acc = acc;
   g.async4 = (c.dtype == DWCONV_F32) ? 1 : 0;  // fp32 pointers are 4-byte aligned
@@ -641,7 +649,7 @@ cudaError_t launch_dconv(const Conv& c, const LCfg& g0, int threads, const void*
     per_sm = 1;
   const int64_t cap = (int64_t)sms * per_sm;
   const int grid = (int)(g.units < cap ? g.units : cap);
-  kern<<<grid, threads, smem, s>>>(c, g, in, w, bias, out);
+  kern<<<grid, threads, smem, s>>>(c, g, in, w, bias, out, ep);
   return cudaGetLastError();
 }
 
@@ -649,7 +657,7 @@ cudaError_t launch_dconv(const Conv& c, const LCfg& g0, int threads, const void*
 // the one with two stages, then four rows (fewer filter-row loads).
 template <int K>
 cudaError_t run_fwd_k(const Conv& c, const void* in, const void* w, const void* bias, void* out, bool flip,
-                      bool acc, cudaStream_t s) {
+                      bool acc, cudaStream_t s, const Epi& ep) {
   LCfg g2, g4;
   int t2 = 0, t4 = 0;
   const bool ok2 = plan_dconv<K, 2>(c, flip, &g2, &t2);
@@ -671,8 +679,8 @@ cudaError_t run_fwd_k(const Conv& c, const void* in, const void* w, const void* 
   } else {
     use4 = !ok2;
   }
-  if (use4) return launch_dconv<K, 4>(c, g4, t4, in, w, bias, out, acc, s);
-  return launch_dconv<K, 2>(c, g2, t2, in, w, bias, out, acc, s);
+  if (use4) return launch_dconv<K, 4>(c, g4, t4, in, w, bias, out, acc, s, ep);
+  return launch_dconv<K, 2>(c, g2, t2, in, w, bias, out, acc, s, ep);
 }
 
 // Shared-memory plan of the weight gradient (host; also used by the
@@ -733,11 +741,12 @@ cudaError_t run_wgrad_k(const Conv& c, const void* x, const void* gy, float* ws,
 // Per-K entry points: one translation unit per K (large_kNN.cu) defines them
 // with this macro; large_entries.h declares them.
 #define DW_LARGE_DEFINE(K)                                                                                   \
-  cudaError_t fwd_k##K(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s) { \
-    return run_fwd_k<K>(c, x, w, b, y, false, false, s);                                                    \
+  cudaError_t fwd_k##K(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s,   \
+                       const Epi& ep) {                                                                     \
+    return run_fwd_k<K>(c, x, w, b, y, false, false, s, ep);                                                \
   }                                                                                                         \
   cudaError_t bwd_k##K(const Conv& c, const void* gy, const void* w, void* gx, bool acc, cudaStream_t s) {  \
-    return run_fwd_k<K>(c, gy, w, nullptr, gx, true, acc, s);                                               \
+    return run_fwd_k<K>(c, gy, w, nullptr, gx, true, acc, s, Epi{});                                        \
   }                                                                                                         \
   cudaError_t wgrad_k##K(const Conv& c, const void* x, const void* gy, float* ws, int chunks,              \
                          cudaStream_t s) {                                                                  \

@@ -36,11 +36,12 @@ const char* algo_name(Algo a) {
   return "unknown";
 }
 
-Algo plan_fwd(const Conv& c) {
+Algo plan_fwd(const Conv& c, bool epilogue) {
   if (force_generic()) return Algo::Generic;
-  if (plane::fwd_supported(c)) return Algo::Plane;
+  // the small-plane and tensor-core kernels have no fused epilogue
+  if (!epilogue && plane::fwd_supported(c)) return Algo::Plane;
   if (tile::fwd_supported(c)) return Algo::Tile;
-  if (allow_ibgemm() && ibg::fwd_supported(c)) return Algo::IBGemm;
+  if (!epilogue && allow_ibgemm() && ibg::fwd_supported(c)) return Algo::IBGemm;
   if (large::supported(c)) return Algo::Large;
   return Algo::Generic;
 }
@@ -71,18 +72,19 @@ WPlan plan_bwd_weight(const Conv& c) {
 }
 
 cudaError_t run_fwd(Algo a, const Conv& c, const void* x, const void* w, const void* b, void* y,
-                    cudaStream_t s) {
+                    cudaStream_t s, const Epi& ep) {
   switch (a) {
     case Algo::Plane: return plane::fwd(c, x, w, b, y, s);
-    case Algo::Tile: return tile::fwd(c, x, w, b, y, s);
-    case Algo::Large: return large::fwd(c, x, w, b, y, s);
+    case Algo::Tile: return tile::fwd(c, x, w, b, y, s, ep);
+    case Algo::Large: return large::fwd(c, x, w, b, y, s, ep);
     case Algo::IBGemm: {
-      // a misaligned pointer rules the tensor-core kernel out for this call only
-      const cudaError_t e = ibg::fwd(c, x, w, b, y, s);
+      // a misaligned pointer rules the tensor-core kernel out for this call
+      // only; it has no fused epilogue
+      const cudaError_t e = ep.active() ? cudaErrorNotSupported : ibg::fwd(c, x, w, b, y, s);
       if (e != cudaErrorNotSupported) return e;
-      return large::supported(c) ? large::fwd(c, x, w, b, y, s) : fwd_generic(c, x, w, b, y, s);
+      return large::supported(c) ? large::fwd(c, x, w, b, y, s, ep) : fwd_generic(c, x, w, b, y, s, ep);
     }
-    default: return fwd_generic(c, x, w, b, y, s);
+    default: return fwd_generic(c, x, w, b, y, s, ep);
   }
 }
 

@@ -22,12 +22,12 @@ struct WPlan {
 };
 
 const char* algo_name(Algo a);
-Algo plan_fwd(const Conv& c);
+Algo plan_fwd(const Conv& c, bool epilogue = false);
 Algo plan_bwd_data(const Conv& c);
 WPlan plan_bwd_weight(const Conv& c);
 
 cudaError_t run_fwd(Algo a, const Conv& c, const void* x, const void* w, const void* b, void* y,
-                    cudaStream_t s);
+                    cudaStream_t s, const Epi& ep = Epi{});
 cudaError_t run_bwd_data(Algo a, const Conv& c, const void* gy, const void* w, void* gx,
                          bool accumulate, cudaStream_t s);
 cudaError_t run_bwd_weight(const WPlan& p, const Conv& c, const void* x, const void* gy, void* gw,
@@ -40,7 +40,8 @@ cudaError_t run_bwd_data_multi(int nb, const Conv* cs, const void* gy, const voi
 namespace tile {
 // tile_fwd.cu
 bool fwd_supported(const Conv& c);
-cudaError_t fwd(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s);
+cudaError_t fwd(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s,
+                const Epi& ep = Epi{});
 bool bwd1_supported(const Conv& c);
 cudaError_t bwd1(const Conv& c, const void* gy, const void* w, void* gx, bool acc, cudaStream_t s);
 // tile_bwd2.cu
@@ -65,7 +66,8 @@ namespace large {
 // large.cu: large-kernel direct convolution (fp32 FMA), stride 1
 bool supported(const Conv& c);
 bool wgrad_supported(const Conv& c);  // supported() and the weight-gradient stages fit shared memory
-cudaError_t fwd(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s);
+cudaError_t fwd(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s,
+                const Epi& ep = Epi{});
 cudaError_t bwd_data(const Conv& c, const void* gy, const void* w, void* gx, bool acc, cudaStream_t s);
 int wgrad_chunks(const Conv& c);
 cudaError_t wgrad(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s);

@@ -9,7 +9,8 @@ namespace dwconv {
 namespace tile {
 
 template <typename T>
-cudaError_t fwd_t(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s);
+cudaError_t fwd_t(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s,
+                  const Epi& ep);
 template <typename T>
 cudaError_t bwd1_t(const Conv& c, const void* gy, const void* w, void* gx, bool acc, cudaStream_t s);
 
@@ -31,9 +32,10 @@ bool fwd_supported(const Conv& c) {
   return false;
 }
 
-cudaError_t fwd(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s) {
+cudaError_t fwd(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s,
+                const Epi& ep) {
   cudaError_t e = cudaErrorInvalidConfiguration;
-  DWCONV_DISPATCH_DTYPE(c.dtype, T, e = fwd_t<T>(c, x, w, b, y, s));
+  DWCONV_DISPATCH_DTYPE(c.dtype, T, e = fwd_t<T>(c, x, w, b, y, s, ep));
   return e;
 }
 

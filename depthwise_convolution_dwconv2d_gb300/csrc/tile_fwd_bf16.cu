@@ -3,6 +3,7 @@
 
 namespace dwconv {
 namespace tile {
-template cudaError_t fwd_t<__nv_bfloat16>(const Conv&, const void*, const void*, const void*, void*, cudaStream_t);
+template cudaError_t fwd_t<__nv_bfloat16>(const Conv&, const void*, const void*, const void*, void*, cudaStream_t,
+                                 const Epi&);
 }  // namespace tile
 }  // namespace dwconv

@@ -28,7 +28,7 @@ template <typename T, int K, int S, int D, int R, int V, int DL>
 __global__ void __launch_bounds__(kNT)
 fwd_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned int* timeouts,
            const T* __restrict__ x, const T* __restrict__ w, const T* __restrict__ bias,
-           T* __restrict__ y) {
+           T* __restrict__ y, Epi ep) {
   extern __shared__ __align__(16) unsigned char smdyn[];
   __shared__ __align__(8) uint64_t bars[2];
   constexpr int Q = Geo<K, S, D>::Q;
@@ -69,8 +69,10 @@ fwd_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned int
     }
     float* wt = tab;
     float* bt = tab + nout * (K * K);
+    float* st = bt + nout;  // epilogue scale and shift (when one is fused)
+    float* ht = st + nout;
     int64_t* ot = reinterpret_cast<int64_t*>(tab + g.tab_off64);
-    // one output plane per thread: its taps, bias and output offset
+    // one output plane per thread: its taps, bias, epilogue and output offset
     for (int pj = threadIdx.x; pj < np * c.m; pj += kNT) {
       const int pl = c.m == 1 ? pj : pj / c.m;
       int64_t n, ch;
@@ -81,6 +83,12 @@ fwd_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned int
       for (int tap = 0; tap < K * K; ++tap) tab_put(wt + pj * (K * K) + tap, wp + tap);
       if (bias) tab_put(bt + pj, bias + oc);
       else bt[pj] = 0.f;
+      if (ep.active()) {
+        if (ep.scale) tab_put(st + pj, reinterpret_cast<const T*>(ep.scale) + oc);
+        else st[pj] = 1.f;
+        if (ep.shift) tab_put(ht + pj, reinterpret_cast<const T*>(ep.shift) + oc);
+        else ht[pj] = 0.f;
+      }
       ot[pj] = c.y_base(n, oc);
     }
   };
@@ -140,6 +148,13 @@ fwd_kernel(Conv c, Cfg g, const __grid_constant__ CUtensorMap tmap, unsigned int
                                            ohr * S - c.ph, owb * S - c.pw, wr, acc);
       } else {
         conv_block<K, S, D, R, V, Q, DL>(cur + (pj / c.m) * g.tile_elems, g.pitch, ohr * S, owb * S + g.cshift, wr, acc);
+      }
+      if (ep.active()) {
+        const float sc = bt[nout + pj], sh = bt[2 * nout + pj];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int v = 0; v < V; ++v) acc[r][v] = epi_act(fmaf(acc[r][v], sc, sh), ep.act);
       }
       store_block<T, R, V, Q>(y + ot[pj], c.Wo, oh0 + ohr, owb, band_rows - ohr, (int)c.Wo, acc,
                               g.vec_out, false);
@@ -281,20 +296,21 @@ template <int K, int S> struct Blk { static constexpr int R = S == 1 ? 4 : 2, V 
 
 template <typename T, int K, int S, int D, int DL>
 cudaError_t launch_fwd(const Conv& c, const Cfg& g, const CUtensorMap& map, const void* x, const void* w,
-                       const void* b, void* y, cudaStream_t s) {
+                       const void* b, void* y, cudaStream_t s, const Epi& ep) {
   constexpr int R = Blk<K, S>::R, V = Blk<K, S>::V;
   auto kern = fwd_kernel<T, K, S, D, R, V, DL>;
   const size_t smem = 128 + 2 * ((size_t)g.stage_elems + g.stg_elems) * sizeof(T) + 2 * (size_t)g.tab_floats * 4;
   cudaError_t e = set_smem(kern, smem);
   if (e != cudaSuccess) return e;
   const int grid = persistent_grid(kern, smem, g.groups * g.nbands);
-  kern<<<grid, kNT, smem, s>>>(c, g, map, tma::timeout_counter(), (const T*)x, (const T*)w, (const T*)b, (T*)y);
+  kern<<<grid, kNT, smem, s>>>(c, g, map, tma::timeout_counter(), (const T*)x, (const T*)w, (const T*)b, (T*)y,
+                               ep);
   return cudaGetLastError();
 }
 
 template <typename T, int K, int S, int D>
 cudaError_t run_fwd_t(const Conv& c, const void* x, const void* w, const void* b, void* y,
-                      cudaStream_t s) {
+                      cudaStream_t s, const Epi& ep) {
   constexpr int R = Blk<K, S>::R, V = Blk<K, S>::V, Q = Geo<K, S, D>::Q;
   const bool vout = Q == 1 && c.Wo % 4 == 0 && alignedn(y, 4 * sizeof(T));
   Cfg g;
@@ -306,10 +322,10 @@ cudaError_t run_fwd_t(const Conv& c, const void* x, const void* w, const void* b
   g.contig = g.mode == kCopyDense;  // x planes n*C + c are contiguous
 
   switch (dl) {
-    case 0: return launch_fwd<T, K, S, D, 0>(c, g, map, x, w, b, y, s);
-    case 1: return launch_fwd<T, K, S, D, Q == 1 ? 1 : 0>(c, g, map, x, w, b, y, s);
-    case 2: return launch_fwd<T, K, S, D, Q == 1 ? 2 : 0>(c, g, map, x, w, b, y, s);
-    default: return launch_fwd<T, K, S, D, Q == 1 ? 3 : 0>(c, g, map, x, w, b, y, s);
+    case 0: return launch_fwd<T, K, S, D, 0>(c, g, map, x, w, b, y, s, ep);
+    case 1: return launch_fwd<T, K, S, D, Q == 1 ? 1 : 0>(c, g, map, x, w, b, y, s, ep);
+    case 2: return launch_fwd<T, K, S, D, Q == 1 ? 2 : 0>(c, g, map, x, w, b, y, s, ep);
+    default: return launch_fwd<T, K, S, D, Q == 1 ? 3 : 0>(c, g, map, x, w, b, y, s, ep);
   }
 }
 
@@ -354,8 +370,9 @@ cudaError_t run_bwd1_t(const Conv& c, const void* gy, const void* w, void* gx, b
 }  // namespace
 
 template <typename T>
-cudaError_t fwd_t(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s) {
-#define X(K, S, D) if (c.kh == K && c.sh == S && c.dh == D) return run_fwd_t<T, K, S, D>(c, x, w, b, y, s);
+cudaError_t fwd_t(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s,
+                  const Epi& ep) {
+#define X(K, S, D) if (c.kh == K && c.sh == S && c.dh == D) return run_fwd_t<T, K, S, D>(c, x, w, b, y, s, ep);
   DW_FWD_CASES(X)
 #undef X
   return cudaErrorInvalidConfiguration;

@@ -129,9 +129,10 @@ bool plan_tile(int64_t nplanes, int ntile, int mult, int64_t Hin, int64_t Win, i
   g.tma_bytes = (uint32_t)((int64_t)g.ppc * ntile * g.tile_elems * ES);
   g.stg_elems = g.mode == kCopyDense ? stage_round((int64_t)g.ppc * ntile * g.seg, ES) : 0;
   // side table: K*K filter taps per staged plane (per output plane for the
-  // forward: mult * ppc of them), one bias each, one 64-bit offset each
+  // forward: mult * ppc of them), a bias, an epilogue scale and shift and a
+  // 64-bit offset each
   const int ntab = g.ppc * (ntile > mult ? ntile : mult);
-  g.tab_off64 = round_up((int64_t)ntab * (K * K + 1), 2);
+  g.tab_off64 = round_up((int64_t)ntab * (K * K + 3), 2);
   g.tab_floats = round_up(g.tab_off64 + 2 * (int64_t)ntab, 4);
   g.vec_out = out_vec_ok;
   g.trdiv = FastDiv((uint32_t)g.tr);

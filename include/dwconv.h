@@ -71,6 +71,13 @@ typedef enum {
   DWCONV_BF16 = 2
 } dwconv_dtype_t;
 
+/* Activation of the fused forward epilogue (dwconv2d_fwd_epilogue). */
+typedef enum {
+  DWCONV_ACT_NONE = 0,
+  DWCONV_ACT_RELU = 1,   /* max(v, 0) */
+  DWCONV_ACT_RELU6 = 2   /* min(max(v, 0), 6) */
+} dwconv_act_t;
+
 typedef enum {
   DWCONV_OK = 0,
   DWCONV_ERR_INVALID_ARG = 1,   /* null pointer, bad size, Ho or Wo < 1, slice out of range */
@@ -154,6 +161,25 @@ dwconv_status_t dwconv2d_bwd_weight_noalloc(const dwconv2d_desc_t* desc, const v
                                             const void* gy, void* gw, void* gbias,
                                             cudaStream_t stream);
 
+/* Forward with a fused epilogue: y = act(scale[oc] * (conv + bias[oc]) +
+ * shift[oc]) for every output channel oc of the descriptor, computed in fp32
+ * and rounded once to the storage type. With scale = gamma / sqrt(var + eps)
+ * and shift = beta - mean * scale it is a convolution followed by an
+ * inference batch norm and an activation in one pass over y. (Source: the
+ * Megvii article "黑科技：用cutlass进行低成本、高性能卷积算子定制开发"
+ * (custom convolution operators with cutlass), its opening list of what the
+ * basic operator libraries lack: a user cannot add a new activation to
+ * their convolution.)
+ * scale and shift are C*m values of desc->dtype (either may be NULL: 1 / 0);
+ * act is a dwconv_act_t (DWCONV_ERR_INVALID_ARG otherwise). Same arguments,
+ * layouts, slices and errors as dwconv2d_fwd otherwise; with NULL scale and
+ * shift and DWCONV_ACT_NONE it is dwconv2d_fwd. The small-plane and
+ * tensor-core forward kernels have no epilogue, so shapes they would serve
+ * run on the tile, direct or generic kernels here. */
+dwconv_status_t dwconv2d_fwd_epilogue(const dwconv2d_desc_t* desc, const void* x, const void* w,
+                                      const void* bias, const void* scale, const void* shift,
+                                      int act, void* y, cudaStream_t stream);
+
 /* Fused multi-branch forward (the DynamicConvolutionOperator's single launch
  * for dilation 1, 3, 5 whose results are stored straight into slices of one
  * concatenated tensor): nbranch (1..8) descriptors over the same x. All
@@ -178,7 +204,8 @@ dwconv_status_t dwconv2d_bwd_data_multi(int nbranch, const dwconv2d_desc_t* desc
 const char* dwconv_status_string(dwconv_status_t status);
 
 /* Name of the kernel family the planner picks for a pass (0 = fwd,
- * 1 = bwd_data, 2 = bwd_weight) of this descriptor: "plane" (3x3 on small
+ * 1 = bwd_data, 2 = bwd_weight, 3 = dwconv2d_fwd_epilogue with a scale, a
+ * shift or an activation) of this descriptor: "plane" (3x3 on small
  * planes, one warp per group of whole planes), "tile" (small filters),
  * "large" (large-filter direct convolution), "ibgemm" (large-filter fp16 /
  * bf16 forward and grad-input as an implicit batched GEMM on the tensor

@@ -100,6 +100,36 @@ def test_null_and_misaligned_pointers(lib):
     assert status_of(B.dwconv2d_bwd_data, d, P, P, P + 2, 0, 0) == MISALIGNED
 
 
+def test_epilogue_argument_checks(lib):
+    d = B.make_desc(2, 3, 8, 8, 3, 1, 1)
+    fe = B.dwconv2d_fwd_epilogue
+    assert status_of(fe, d, P, P, None, None, None, 3, P, 0) == INVALID     # unknown activation
+    assert status_of(fe, d, P, P, None, None, None, -1, P, 0) == INVALID
+    assert status_of(fe, d, P, P, None, P + 2, None, "relu", P, 0) == MISALIGNED   # scale
+    assert status_of(fe, d, P, P, None, None, P + 1, "relu6", P, 0) == MISALIGNED  # shift
+    assert status_of(fe, d, None, P, None, P, P, "relu", P, 0) == INVALID
+    assert status_of(fe, d, P, P, None, P, P, "relu", None, 0) == INVALID
+    # empty batch: a valid no-op once the filter pointers check out
+    e = B.make_desc(0, 3, 8, 8, 3, 1, 1)
+    assert status_of(fe, e, None, P, None, P, P, "relu", None, 0) == 0
+
+
+def test_epilogue_plan_avoids_kernels_without_one(lib):
+    """Pass 3 (forward with a fused epilogue) never names the small-plane or
+    tensor-core forward kernels, which have no epilogue."""
+    small = B.make_desc(64, 512, 14, 14, 3, 1, 1)
+    assert B.dwconv2d_plan_name(small, 0) == "plane"
+    assert B.dwconv2d_plan_name(small, 3) == "tile"
+    big = B.make_desc(64, 384, 32, 32, 31, 1, 15, dtype="f16")
+    assert B.dwconv2d_plan_name(big, 0) == "ibgemm"
+    assert B.dwconv2d_plan_name(big, 3) == "large"
+    mb = B.make_desc(64, 128, 56, 56, 3, 1, 1)
+    assert B.dwconv2d_plan_name(mb, 3) == B.dwconv2d_plan_name(mb, 0) == "tile"
+    odd = B.make_desc(2, 3, 9, 9, 4, 1, 1)
+    assert B.dwconv2d_plan_name(odd, 3) == "generic"
+    assert B.dwconv2d_plan_name(odd, 4) == "invalid"
+
+
 def test_workspace_checks(lib):
     d = B.make_desc(4, 8, 16, 16, 3, 1, 1)
     need = B.dwconv2d_bwd_weight_workspace_size(d)
@@ -141,7 +171,8 @@ def test_status_strings(lib):
 
 def test_plan_names(lib):
     assert B.dwconv2d_plan_name(B.make_desc(64, 128, 56, 56, 3, 1, 1), 0) in ("generic", "tile", "large")
-    assert B.dwconv2d_plan_name(B.make_desc(64, 128, 56, 56, 3, 1, 1), 3) == "invalid"
+    assert B.dwconv2d_plan_name(B.make_desc(64, 128, 56, 56, 3, 1, 1), 4) == "invalid"
+    assert B.dwconv2d_plan_name(B.make_desc(64, 128, 56, 56, 3, 1, 1), -1) == "invalid"
 
 
 def test_plane_routing_and_chunking(lib):

@@ -1,0 +1,125 @@
+"""GPU parity of the fused forward variants against the fp64 oracle.
+
+dwconv2d_fwd_epilogue: y = act(scale * (conv + bias) + shift) per output
+channel, for every kernel family the planner can route it to (tile, large,
+generic), with channel slices, ragged planes and each activation. Scale and
+shift are a folded inference batch norm drawn from fixed seeds.
+Tolerances as in the other parity tests: fp32 normwise max|g-r|/max|r| <=
+1e-5 sqrt(taps); fp16/bf16 elementwise |g-r| <= 1e-2 + 2e-2 |r|.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from depthwise_convolution_dwconv2d_gb300 import binding as B
+from depthwise_convolution_dwconv2d_gb300 import synth, workloads as WL
+from dw_testutil import assert_close, empty_dev, oconv, to_dev, to_f64, torch
+
+pytestmark = pytest.mark.gpu
+
+# seeded streams of the batch-norm statistics (distinct from x, w, b, gy)
+STREAM_GAMMA, STREAM_BETA, STREAM_MEAN, STREAM_VAR = 40, 41, 42, 43
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    th = pytest.importorskip("torch")
+    if not th.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from depthwise_convolution_dwconv2d_gb300 import build
+    build.build()
+    B.load()
+
+
+def folded_bn(OC, dtype, seed=0):
+    """Per-channel scale / shift of an inference batch norm, rounded to the
+    storage type (the kernels and the oracle both see the rounded values)."""
+    gamma = synth.normal_tensor((OC,), "f32", seed, STREAM_GAMMA, std=0.3).f64 + 1.0
+    beta = synth.normal_tensor((OC,), "f32", seed, STREAM_BETA, std=0.5).f64
+    mean = synth.normal_tensor((OC,), "f32", seed, STREAM_MEAN, std=0.2).f64
+    var = synth.uniform_tensor((OC,), "f32", seed, STREAM_VAR, lo=0.25, hi=1.0).f64
+    scale = gamma / np.sqrt(var + 1e-5)
+    shift = beta - mean * scale
+    return synth.Tensor(scale, (OC,), dtype), synth.Tensor(shift, (OC,), dtype)
+
+
+EPI_CASES = [
+    (WL.Layer(N=4, C=64, H=28, W=28, k=3, s=1, p=1, bias=True), "relu6", "tile"),
+    (WL.Layer(N=2, C=32, H=57, W=57, k=3, s=2, p=1, dtype="bf16"), "relu", "tile"),
+    (WL.Layer(N=3, C=24, H=20, W=19, k=5, s=1, p=2, m=2, bias=True, dtype="f16"), "none", "tile"),
+    (WL.Layer(N=8, C=32, H=14, W=14, k=3, s=1, p=1), "relu", "tile"),      # small planes
+    (WL.Layer(N=3, C=8, H=40, W=40, k=13, p=6, bias=True), "relu", "large"),
+    (WL.Layer(N=2, C=4, H=32, W=32, k=31, p=15, dtype="f16"), "relu6", "large"),
+    (WL.Layer(N=2, C=5, H=23, W=17, k=4, s=1, p=1, bias=True), "relu", "generic"),
+    (WL.Layer(N=2, C=6, H=21, W=21, k=3, s=1, p=7, d=7, dtype="bf16"), "relu6", "generic"),
+]
+EPI_IDS = ["mb3x3_f32_relu6", "s2_bf16_relu", "m2_f16_slice", "plane_shape_f32", "k13_f32",
+           "k31_f16", "k4_generic", "d7_bf16_generic"]
+
+
+@pytest.mark.parametrize("L,act,family", EPI_CASES, ids=EPI_IDS)
+def test_epilogue_vs_oracle(L, act, family):
+    th = torch()
+    off, ctot = (3, L.OC + 5) if L.m == 2 else (0, 0)
+    d = B.make_desc(**L.desc_kwargs(), out_c_offset=off, out_c_total=ctot)
+    assert B.dwconv2d_plan_name(d, 3) == family
+    inp = WL.make_inputs(L)
+    scale, shift = folded_bn(L.OC, L.dtype)
+    x, w = to_dev(inp.x), to_dev(inp.w)
+    b = to_dev(inp.b) if inp.b is not None else None
+    y = empty_dev((L.N, ctot or L.OC, L.Ho, L.Wo), L.dtype, fill=-7.0)
+    B.dwconv2d_fwd_epilogue(d, x, w, b, to_dev(scale), to_dev(shift), act, y)
+    th.cuda.synchronize()
+    got = to_f64(y)
+    cv = oconv(L, off=off, c_total=ctot or None)
+    ref = np.full(got.shape, -7.0)
+    oracle.fwd_epilogue(cv, inp.x.f64, inp.w.f64, None if inp.b is None else inp.b.f64,
+                        scale.f64, shift.f64, act, y=ref)
+    assert_close(got, ref, L.dtype, L.k * L.k, f"{L.label()} {act}")
+    if act != "none":
+        s = got[:, off:off + L.OC]
+        assert s.min() >= 0.0 and (act != "relu6" or s.max() <= 6.0)
+    if ctot:
+        assert np.all(got[:, :off] == -7.0) and np.all(got[:, off + L.OC:] == -7.0)
+
+
+@pytest.mark.parametrize("L", [EPI_CASES[0][0], EPI_CASES[3][0], EPI_CASES[5][0], EPI_CASES[6][0]],
+                         ids=["tile", "plane_shape", "ibgemm_shape", "generic"])
+def test_epilogue_without_scale_shift_or_activation_is_plain_forward(L):
+    """NULL scale and shift with no activation is dwconv2d_fwd, bit for bit,
+    on whichever kernel the plain forward picks."""
+    th = torch()
+    d = B.make_desc(**L.desc_kwargs())
+    inp = WL.make_inputs(L)
+    x, w = to_dev(inp.x), to_dev(inp.w)
+    b = to_dev(inp.b) if inp.b is not None else None
+    y0 = empty_dev((L.N, L.OC, L.Ho, L.Wo), L.dtype)
+    y1 = empty_dev((L.N, L.OC, L.Ho, L.Wo), L.dtype)
+    B.dwconv2d_fwd(d, x, w, b, y0)
+    B.dwconv2d_fwd_epilogue(d, x, w, b, None, None, "none", y1)
+    th.cuda.synchronize()
+    assert th.equal(y0, y1)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_epilogue_matches_unfused_sequence(dtype):
+    """The fused result equals conv -> (scale, shift) -> ReLU6 done as three
+    fp32 steps in torch on the kernel's own unfused fp32 output, up to the one
+    rounding the fused path saves (the check is of the index mapping of scale
+    and shift, not of the arithmetic)."""
+    th = torch()
+    L = WL.Layer(N=2, C=48, H=33, W=30, k=3, s=1, p=1, bias=True, dtype=dtype)
+    d = B.make_desc(**L.desc_kwargs())
+    inp = WL.make_inputs(L)
+    scale, shift = folded_bn(L.OC, dtype, seed=3)
+    x, w, b = to_dev(inp.x), to_dev(inp.w), to_dev(inp.b)
+    y = empty_dev((L.N, L.OC, L.Ho, L.Wo), dtype)
+    B.dwconv2d_fwd_epilogue(d, x, w, b, to_dev(scale), to_dev(shift), "relu6", y)
+    y0 = empty_dev((L.N, L.OC, L.Ho, L.Wo), dtype)
+    B.dwconv2d_fwd(d, x, w, b, y0)
+    th.cuda.synchronize()
+    sc = th.tensor(scale.f64, dtype=th.float32, device="cuda").view(1, -1, 1, 1)
+    sh = th.tensor(shift.f64, dtype=th.float32, device="cuda").view(1, -1, 1, 1)
+    want = th.clamp(y0.float() * sc + sh, 0.0, 6.0)
+    tol = 1e-5 if dtype == "f32" else 3e-2
+    assert th.allclose(y.float(), want, rtol=tol, atol=tol)
