@@ -2,7 +2,7 @@
 """Benchmark: one step = forward, backward-data and backward-weight of every
 layer of a synthetic depthwise workload, through libdwconv's C ABI.
 
-The five workloads (``depthwise_convolution_dwconv2d_gb300.workloads``):
+The six workloads (``depthwise_convolution_dwconv2d_gb300.workloads``):
   pr1        -- N=1 C=32 28x28 3x3 fp32 ("Spatial Depthwise Convolution on
                 the GPU #3057", its smallest MobileNet layer);
   mobilenet  -- the PR's MobileNet layer table at batch 64, fp32;
@@ -10,10 +10,13 @@ The five workloads (``depthwise_convolution_dwconv2d_gb300.workloads``):
                 (the MegEngine large-kernel article's setting);
   multidil   -- three 3x3 branches with dilation 1/3/5 into one concatenated
                 output, bf16 (the DynamicConvolutionOperator README);
-  multiplier -- 128 x 256 x 28^2, 5x5, multiplier 2, bias, bf16.
+  multiplier -- 128 x 256 x 28^2, 5x5, multiplier 2, bias, bf16;
+  infer      -- the MobileNet table again as an inference forward in
+                channels-last layout with a fused scale / shift / ReLU6
+                epilogue, fp32 and bf16 (forward only: one call per layer).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                    [--workload all|pr1|mobilenet|largek|multidil|multiplier]
+                    [--workload all|pr1|mobilenet|largek|multidil|multiplier|infer]
 
 With no flags every workload is timed, one after another, and ONE JSON line
 is printed (rank 0). Its headline (``value``, ``config``, ``roofline``,
@@ -47,7 +50,7 @@ sys.path.insert(0, ROOT)
 METRIC = "dwconv fwd/bwd-data/bwd-weight ms, achieved GB/s or TFLOP/s vs roofline"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-ORDER = ("pr1", "mobilenet", "largek", "multidil", "multiplier")
+ORDER = ("pr1", "mobilenet", "largek", "multidil", "multiplier", "infer")
 HEADLINE = "largek"
 WORKLOAD_TEXT = {
     "pr1": "PR1 layer, fp32 NCHW, N=1 C=32 H=W=28, 3x3, stride 1, pad 1, fwd+bwd_data+bwd_weight",
@@ -60,6 +63,8 @@ WORKLOAD_TEXT = {
                 "one N x 3C x H x W output; fwd + bwd_data (branch sum) + bwd_weight per branch",
     "multiplier": "Depth-multiplier layer, bf16, N=128 C=256 H=W=28, m=2 (512 out channels), 5x5 pad 2, bias; "
                   "fwd+bwd_data+bwd_weight+bias grad",
+    "infer": "MobileNet-shape inference forward, channels-last (NHWC in and out), N=64, 3x3 pad 1, fused "
+             "per-channel scale + shift + ReLU6 (a folded batch norm), fp32 and bf16; same layer table as mobilenet",
 }
 # Source files whose device code each kernel family runs: a committed DRAM
 # traffic figure is reported only while these files are unchanged.
@@ -72,6 +77,7 @@ FAMILY_SOURCES = {
     "ibgemm": ("common.cuh", "plan.h", "tma.cuh", "tma.cu", "ibgemm.cu"),
     "tcwgrad": ("common.cuh", "plan.h", "tma.cuh", "tma.cu", "wgrad_tc.cu", "generic.cu"),
     "generic": ("common.cuh", "plan.h", "generic.cu"),
+    "nhwc": ("common.cuh", "plan.h", "nhwc.h", "nhwc.cu", "tile.cuh", "tma.cuh", "tma.cu"),
 }
 
 
@@ -88,6 +94,8 @@ def build_workload(name):
         return WL.multiplier()
     if name == "multidil":
         return [WL.multidil()]
+    if name == "infer":
+        return WL.mobilenet_infer()
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -118,6 +126,10 @@ def layer_calls(item):
         return out
     L = item
     es = 4 if L.dtype == "f32" else 2
+    if isinstance(L, WL.InferLayer):
+        fma = L.N * L.OC * valid_taps(L.Ho, L.k, L.s, L.p, L.d, L.H) * valid_taps(L.Wo, L.k, L.s, L.p, L.d, L.W)
+        nb = L.N * L.C * L.H * L.W * es + L.N * L.OC * L.Ho * L.Wo * es + L.OC * (L.k * L.k + 2) * es
+        return [("fwd", nb + (L.OC * es if L.bias else 0), fma, 1)]
     xb = L.N * L.C * L.H * L.W * es
     yb = L.N * L.OC * L.Ho * L.Wo * es
     wb = L.OC * L.k * L.k * es
@@ -295,16 +307,23 @@ def oracle_sample(items, budget_s):
                     bytes_total += b
                     fma_total += f
                 continue
-            L = WL.Layer(**{**item.__dict__, "N": n, "C": C})
+            L = type(item)(**{**item.__dict__, "N": n, "C": C})
             inp = WL.make_inputs(L)
             cv = oracle.Conv(N=n, C=L.C, H=L.H, W=L.W, kh=L.k, kw=L.k, sh=L.s, sw=L.s, ph=L.p, pw=L.p,
                              dh=L.d, dw=L.d, m=L.m)
             b = inp.b.f64 if inp.b is not None else None
-            t0 = time.perf_counter()
-            oracle.fwd(cv, inp.x.f64, inp.w.f64, b)
-            oracle.bwd_data(cv, inp.gy.f64, inp.w.f64)
-            oracle.bwd_weight(cv, inp.x.f64, inp.gy.f64, want_b=L.bias)
-            t_total += time.perf_counter() - t0
+            if isinstance(L, WL.InferLayer):
+                # the oracle is layout-free: NCHW arrays, the same function
+                sc, sh = WL.make_scale_shift(L)
+                t0 = time.perf_counter()
+                oracle.fwd_epilogue(cv, inp.x.f64, inp.w.f64, b, sc.f64, sh.f64, L.act)
+                t_total += time.perf_counter() - t0
+            else:
+                t0 = time.perf_counter()
+                oracle.fwd(cv, inp.x.f64, inp.w.f64, b)
+                oracle.bwd_data(cv, inp.gy.f64, inp.w.f64)
+                oracle.bwd_weight(cv, inp.x.f64, inp.gy.f64, want_b=L.bias)
+                t_total += time.perf_counter() - t0
             for _, bb, f, _ in layer_calls(L):
                 bytes_total += bb
                 fma_total += f
@@ -325,8 +344,9 @@ def oracle_sample(items, budget_s):
             c = full_c
             n = max(1, min(full_n, int(scale)))
         t, by, fm = run(n, c)
+    passes = "fwd with epilogue" if all(isinstance(i, WL.InferLayer) for i in items) else "fwd+bwd_data+bwd_weight"
     desc = (f"first {n} sample(s)" + ("" if c >= full_c else f" and first {c} channels") +
-            " of every layer, fwd+bwd_data+bwd_weight, one timed pass")
+            f" of every layer, {passes}, one timed pass")
     return by / t, fm / t, t, desc
 
 
@@ -340,6 +360,15 @@ def cpu_baseline(name, items, budget_s, unit):
 
 
 # ------------------------------------------------------------------ GPU arm
+class _NHWC:
+    """A synthetic NCHW tensor's bytes transposed to channels-last."""
+
+    def __init__(self, t):
+        import numpy as np
+        self.dtype = t.dtype
+        self.store = np.ascontiguousarray(t.store.transpose(0, 2, 3, 1))
+
+
 class HostCache:
     """Synthetic host tensors, drawn once per (shape, dtype, stream, std) and
     pinned; layers with equal shapes share them (the device buffers are still
@@ -421,6 +450,22 @@ def setup_workload(name, items, dev, stream, hc, out_host):
         L = item
         xd = "uniform" if L.x_dist == "uniform" else "normal"
         wstd = L.w_std if L.w_std is not None else 1.0 / L.k
+        if isinstance(L, WL.InferLayer):
+            xh = hc.get(("x_nhwc", (L.N, L.H, L.W, L.C), L.dtype, xd), lambda L=L: _NHWC(WL.make_x(L)))
+            wh = hc.get(("w", (L.OC, L.k, L.k), L.dtype, 0, wstd), lambda L=L: WL.make_w(L))
+            sch = hc.get(("scale", (L.OC,), L.dtype), lambda L=L: WL.make_scale_shift(L)[0])
+            shh = hc.get(("shift", (L.OC,), L.dtype), lambda L=L: WL.make_scale_shift(L)[1])
+            d = B.make_desc(**L.desc_kwargs())
+            x, w, sc, sh = xh.to(dev), wh.to(dev), sch.to(dev), shh.to(dev)
+            y = torch.empty((L.N, L.Ho, L.Wo, L.OC), dtype=tdt(L.dtype), device=dev)
+            cl = layer_calls(L)
+            idx0 = len(calls)
+            calls.append(("fwd", L.label(), fam(B.dwconv2d_plan_name(d, 4), L.dtype), cl[0][1], cl[0][2], 1,
+                          lambda d=d, x=x, w=w, y=y, sc=sc, sh=sh, act=L.act:
+                          B.dwconv2d_fwd_nhwc(d, x, w, None, y, sc, sh, act, stream)))
+            h2d = [(xh, x), (wh, w), (sch, sc), (shh, sh)]
+            groups.append((h2d, list(range(idx0, len(calls))), [(y, host_out(y))]))
+            continue
         xh = hc.get(("x", (L.N, L.C, L.H, L.W), L.dtype, xd), lambda L=L: WL.make_x(L))
         wh = hc.get(("w", (L.OC, L.k, L.k), L.dtype, 0, wstd), lambda L=L: WL.make_w(L))
         gyh = hc.get(("gy", (L.N, L.OC, L.Ho, L.Wo), L.dtype), lambda L=L: WL.make_gy(L))

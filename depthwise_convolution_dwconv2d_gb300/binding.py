@@ -24,7 +24,8 @@ SYMBOLS = ("dwconv2d_output_shape", "dwconv2d_fwd", "dwconv2d_bwd_data",
            "dwconv2d_bwd_weight_workspace_size", "dwconv2d_bwd_weight", "dwconv2d_fwd_multi",
            "dwconv2d_bwd_data_multi", "dwconv_status_string", "dwconv2d_plan_name",
            "dwconv2d_multi_plan_name", "dwconv_fma_probe", "dwconv2d_bwd_weight_noalloc",
-           "dwconv_device_timeouts", "dwconv_wait_selftest", "dwconv2d_fwd_epilogue")
+           "dwconv_device_timeouts", "dwconv_wait_selftest", "dwconv2d_fwd_epilogue",
+           "dwconv2d_fwd_nhwc")
 
 # dwconv_act_t
 ACTS = {"none": 0, "relu": 1, "relu6": 2}
@@ -86,6 +87,7 @@ def load():
     lib.dwconv2d_output_shape.argtypes = [P, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]
     lib.dwconv2d_fwd.argtypes = [P, vp, vp, vp, vp, vp]
     lib.dwconv2d_fwd_epilogue.argtypes = [P, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp]
+    lib.dwconv2d_fwd_nhwc.argtypes = [P, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp]
     lib.dwconv2d_bwd_data.argtypes = [P, vp, vp, vp, ctypes.c_int, vp]
     lib.dwconv2d_bwd_weight_workspace_size.argtypes = [P]
     lib.dwconv2d_bwd_weight_workspace_size.restype = ctypes.c_size_t
@@ -154,6 +156,14 @@ def dwconv2d_fwd_epilogue(desc: Desc, x, w, bias, scale, shift, act, y, stream=N
     _check(load().dwconv2d_fwd_epilogue(ctypes.byref(desc), _ptr(x), _ptr(w), _ptr(bias), _ptr(scale),
                                          _ptr(shift), a, _ptr(y), _stream(stream)),
            "dwconv2d_fwd_epilogue")
+
+
+def dwconv2d_fwd_nhwc(desc: Desc, x, w, bias, y, scale=None, shift=None, act=0, stream=None):
+    """x [N, H, W, C], y [N, Ho, Wo, out_c_total]; optional fused epilogue."""
+    a = ACTS[act] if isinstance(act, str) else int(act)
+    _check(load().dwconv2d_fwd_nhwc(ctypes.byref(desc), _ptr(x), _ptr(w), _ptr(bias), _ptr(scale),
+                                     _ptr(shift), a, _ptr(y), _stream(stream)),
+           "dwconv2d_fwd_nhwc")
 
 
 def dwconv2d_bwd_data(desc: Desc, gy, w, gx, accumulate=0, stream=None):

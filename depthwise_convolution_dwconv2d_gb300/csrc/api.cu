@@ -11,6 +11,7 @@
 #include <cstring>
 
 #include "common.cuh"
+#include "nhwc.h"
 #include "plan.h"
 
 namespace dwconv {
@@ -131,8 +132,9 @@ dwconv_status_t dwconv2d_output_shape(const dwconv2d_desc_t* desc, int64_t* Ho, 
 
 const char* dwconv2d_plan_name(const dwconv2d_desc_t* desc, int pass) {
   Conv c;
-  if (make_conv(desc, &c) != DWCONV_OK || pass < 0 || pass > 3) return "invalid";
+  if (make_conv(desc, &c) != DWCONV_OK || pass < 0 || pass > 4) return "invalid";
   if (pass == 3) return algo_name(plan_fwd(c, true));
+  if (pass == 4) return algo_name(nhwc::plan(c));
   return algo_name(pass == 0 ? plan_fwd(c) : pass == 1 ? plan_bwd_data(c) : plan_bwd_weight(c).algo);
 }
 
@@ -172,6 +174,24 @@ dwconv_status_t dwconv2d_fwd_epilogue(const dwconv2d_desc_t* desc, const void* x
   DW_TRY(check_ptr(y, es, true));
   const Epi ep{scale, shift, act};
   return cuda_status(run_fwd(plan_fwd(c, ep.active()), c, x, w, bias, y, stream, ep));
+}
+
+dwconv_status_t dwconv2d_fwd_nhwc(const dwconv2d_desc_t* desc, const void* x, const void* w,
+                                  const void* bias, const void* scale, const void* shift, int act,
+                                  void* y, cudaStream_t stream) {
+  Conv c;
+  DW_TRY(make_conv(desc, &c));
+  if (act != DWCONV_ACT_NONE && act != DWCONV_ACT_RELU && act != DWCONV_ACT_RELU6)
+    return DWCONV_ERR_INVALID_ARG;
+  const int es = esize(c.dtype);
+  DW_TRY(check_ptr(w, es, true));
+  DW_TRY(check_ptr(bias, es, false));
+  DW_TRY(check_ptr(scale, es, false));
+  DW_TRY(check_ptr(shift, es, false));
+  if (c.N == 0) return DWCONV_OK;
+  DW_TRY(check_ptr(x, es, true));
+  DW_TRY(check_ptr(y, es, true));
+  return cuda_status(nhwc::fwd(c, x, w, bias, y, stream, Epi{scale, shift, act}));
 }
 
 dwconv_status_t dwconv2d_bwd_data(const dwconv2d_desc_t* desc, const void* gy, const void* w,

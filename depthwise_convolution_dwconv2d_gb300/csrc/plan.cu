@@ -32,6 +32,7 @@ const char* algo_name(Algo a) {
     case Algo::IBGemm: return "ibgemm";
     case Algo::Plane: return "plane";
     case Algo::TcWgrad: return "tcwgrad";
+    case Algo::Nhwc: return "nhwc";
   }
   return "unknown";
 }

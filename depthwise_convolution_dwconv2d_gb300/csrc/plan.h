@@ -14,6 +14,7 @@ enum class Algo {
   IBGemm = 3,    // ibgemm.cu: large-kernel implicit batched GEMM on tcgen05 (fp16 / bf16)
   Plane = 4,     // plane.cu: 3x3 on small planes, one warp per group of whole planes
   TcWgrad = 5,   // wgrad_tc.cu: large-kernel weight gradient on tcgen05 (fp16 / bf16)
+  Nhwc = 6,      // nhwc.cu: channels-last forward, TMA-staged channel-vector tiles
 };
 
 struct WPlan {

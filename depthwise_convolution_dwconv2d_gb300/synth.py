@@ -17,8 +17,8 @@ oracle, which widens them exactly to float64, so quantisation of the inputs is
 never counted as error.
 
 Stream ids (per tensor, so shapes can change without reshuffling others):
-x = 0, w = 1, bias = 2, gy = 3; branch i > 0 of a multi-branch op uses
-w = 1 + 16 i and bias = 2 + 16 i.
+x = 0, w = 1, bias = 2, gy = 3, epilogue scale = 4, epilogue shift = 5;
+branch i > 0 of a multi-branch op uses w = 1 + 16 i and bias = 2 + 16 i.
 """
 from __future__ import annotations
 
@@ -31,6 +31,7 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
 STREAM_X, STREAM_W, STREAM_B, STREAM_GY = 0, 1, 2, 3
+STREAM_SCALE, STREAM_SHIFT = 4, 5
 
 _CHUNK = 1 << 22
 

@@ -11,7 +11,11 @@ The shapes stand in for the workloads the pages time:
   * "multidil"   -- the DynamicConvolutionOperator's fused dilation 1/3/5
                     branches (dim 64, resolution 256, batch 2), bf16,
                     stored into one concatenated output;
-  * "multiplier" -- a depth-multiplier-2 5x5 training layer with bias, bf16.
+  * "multiplier" -- a depth-multiplier-2 5x5 training layer with bias, bf16;
+  * "infer"      -- the MobileNet layer table as an inference forward in
+                    channels-last layout with a fused per-channel scale,
+                    shift and ReLU6 (a folded batch norm and activation),
+                    fp32 and bf16.
 No public dataset is involved: every tensor is drawn by ``synth`` with seed 0
 and per-tensor streams. Variances are read as variances: N(0, 1/9) has
 standard deviation 1/3.
@@ -93,6 +97,21 @@ def mobilenet(N=64):
     return [Layer(N=N, C=c, H=h, W=h, k=3, s=s, p=1, name=f"mb_C{c}_H{h}_s{s}") for c, h, s in layers]
 
 
+@dataclass
+class InferLayer(Layer):
+    """A forward-only layer: channels-last (NHWC) input and output, with the
+    fused per-channel scale / shift / activation epilogue."""
+    layout: str = "nhwc"
+    act: str = "relu6"
+
+
+def mobilenet_infer(N=64, dtypes=("f32", "bf16")):
+    layers = [(64, 112, 2), (128, 56, 1), (128, 56, 2), (256, 28, 1), (256, 28, 2),
+              (512, 14, 1), (512, 14, 2), (1024, 7, 2)]
+    return [InferLayer(N=N, C=c, H=h, W=h, k=3, s=s, p=1, dtype=dt, name=f"mbi_C{c}_H{h}_s{s}_{dt}")
+            for dt in dtypes for c, h, s in layers]
+
+
 def pr1():
     return [Layer(N=1, C=32, H=28, W=28, k=3, s=1, p=1, name="pr1_C32_H28")]
 
@@ -139,6 +158,12 @@ def make_b(L: Layer, seed: int = 0, branch: int = 0) -> synth.Tensor:
 def make_gy(L: Layer, seed: int = 0, gy_channels: int | None = None) -> synth.Tensor:
     gc = L.OC if gy_channels is None else gy_channels
     return synth.normal_tensor((L.N, gc, L.Ho, L.Wo), L.dtype, seed, synth.STREAM_GY)
+
+
+def make_scale_shift(L: Layer, seed: int = 0):
+    """Epilogue scale ~ U[0.5, 1.5] and shift ~ N(0, 0.25), one per output channel."""
+    return (synth.uniform_tensor((L.OC,), L.dtype, seed, synth.STREAM_SCALE, lo=0.5, hi=1.5),
+            synth.normal_tensor((L.OC,), L.dtype, seed, synth.STREAM_SHIFT, std=0.5))
 
 
 def make_inputs(L: Layer, seed: int = 0, branch: int = 0, gy_channels: int | None = None) -> Inputs:

@@ -180,6 +180,27 @@ dwconv_status_t dwconv2d_fwd_epilogue(const dwconv2d_desc_t* desc, const void* x
                                       const void* bias, const void* scale, const void* shift,
                                       int act, void* y, cudaStream_t stream);
 
+/* Channels-last forward: the same operation and descriptor as dwconv2d_fwd
+ * with the channel axis innermost,
+ *   x : [N, H, W, C]               input, contiguous
+ *   w : [C*m, kh, kw]              filters, as dwconv2d_fwd
+ *   y : [N, Ho, Wo, out_c_total]   output; this call writes channels
+ *                                  [out_c_offset, out_c_offset + C*m) of
+ *                                  every pixel and nothing else
+ * with the fused epilogue of dwconv2d_fwd_epilogue (scale / shift / act;
+ * NULL, NULL, DWCONV_ACT_NONE for none). The layout is PyTorch's
+ * channels_last memory format. (The pages' kernels are NCHW; this variant
+ * is this library's, for callers whose tensors are channels-last, so that
+ * they need no transpose.) Same errors as dwconv2d_fwd_epilogue. 3x3, 5x5
+ * and 7x7 filters with equal strides of 1 or 2, dilation 1, one filter per
+ * channel and C * element size a multiple of 16 bytes run on a tiled
+ * kernel that stages input boxes with the tensor memory accelerator (x must
+ * then be 16-byte aligned, else the generic kernel runs); every other shape
+ * runs on a one-output-per-thread kernel. */
+dwconv_status_t dwconv2d_fwd_nhwc(const dwconv2d_desc_t* desc, const void* x, const void* w,
+                                  const void* bias, const void* scale, const void* shift, int act,
+                                  void* y, cudaStream_t stream);
+
 /* Fused multi-branch forward (the DynamicConvolutionOperator's single launch
  * for dilation 1, 3, 5 whose results are stored straight into slices of one
  * concatenated tensor): nbranch (1..8) descriptors over the same x. All
@@ -205,7 +226,8 @@ const char* dwconv_status_string(dwconv_status_t status);
 
 /* Name of the kernel family the planner picks for a pass (0 = fwd,
  * 1 = bwd_data, 2 = bwd_weight, 3 = dwconv2d_fwd_epilogue with a scale, a
- * shift or an activation) of this descriptor: "plane" (3x3 on small
+ * shift or an activation, 4 = dwconv2d_fwd_nhwc) of this descriptor: "nhwc"
+ * (the tiled channels-last forward), "plane" (3x3 on small
  * planes, one warp per group of whole planes), "tile" (small filters),
  * "large" (large-filter direct convolution), "ibgemm" (large-filter fp16 /
  * bf16 forward and grad-input as an implicit batched GEMM on the tensor

@@ -127,7 +127,28 @@ def test_epilogue_plan_avoids_kernels_without_one(lib):
     assert B.dwconv2d_plan_name(mb, 3) == B.dwconv2d_plan_name(mb, 0) == "tile"
     odd = B.make_desc(2, 3, 9, 9, 4, 1, 1)
     assert B.dwconv2d_plan_name(odd, 3) == "generic"
-    assert B.dwconv2d_plan_name(odd, 4) == "invalid"
+    assert B.dwconv2d_plan_name(odd, 5) == "invalid"
+
+
+def test_nhwc_argument_checks_and_routing(lib):
+    d = B.make_desc(2, 32, 8, 8, 3, 1, 1)
+    fn = B.dwconv2d_fwd_nhwc
+    assert status_of(fn, d, P, P, None, P, None, None, 7) == INVALID          # unknown activation
+    assert status_of(fn, d, P, None, None, P) == INVALID
+    assert status_of(fn, d, P, P, None, None) == INVALID
+    assert status_of(fn, d, P + 2, P, None, P) == MISALIGNED
+    assert status_of(fn, d, P, P, None, P, P + 1, None, "relu") == MISALIGNED
+    assert status_of(fn, B.make_desc(0, 32, 8, 8, 3, 1, 1), None, P, None, None) == 0
+    # tiled kernel: 3/5/7 square, stride 1 or 2, dilation 1, m = 1, C*es % 16 == 0
+    assert B.dwconv2d_plan_name(B.make_desc(64, 128, 56, 56, 3, 1, 1), 4) == "nhwc"
+    assert B.dwconv2d_plan_name(B.make_desc(64, 64, 112, 112, 3, 2, 1, dtype="bf16"), 4) == "nhwc"
+    assert B.dwconv2d_plan_name(B.make_desc(8, 36, 30, 30, 7, 2, 3), 4) == "nhwc"
+    assert B.dwconv2d_plan_name(B.make_desc(8, 6, 30, 30, 3, 1, 1), 4) == "generic"        # 24-byte pixels
+    assert B.dwconv2d_plan_name(B.make_desc(8, 12, 30, 30, 3, 1, 1, dtype="f16"), 4) == "generic"
+    assert B.dwconv2d_plan_name(B.make_desc(8, 32, 30, 30, 3, 1, 2, 2), 4) == "generic"    # dilation
+    assert B.dwconv2d_plan_name(B.make_desc(8, 32, 30, 30, 3, 3, 1), 4) == "generic"       # stride 3
+    assert B.dwconv2d_plan_name(B.make_desc(8, 32, 30, 30, 3, 1, 1, multiplier=2), 4) == "generic"
+    assert B.dwconv2d_plan_name(B.make_desc(8, 32, 30, 30, 9, 1, 4), 4) == "generic"
 
 
 def test_workspace_checks(lib):
@@ -171,7 +192,7 @@ def test_status_strings(lib):
 
 def test_plan_names(lib):
     assert B.dwconv2d_plan_name(B.make_desc(64, 128, 56, 56, 3, 1, 1), 0) in ("generic", "tile", "large")
-    assert B.dwconv2d_plan_name(B.make_desc(64, 128, 56, 56, 3, 1, 1), 4) == "invalid"
+    assert B.dwconv2d_plan_name(B.make_desc(64, 128, 56, 56, 3, 1, 1), 5) == "invalid"
     assert B.dwconv2d_plan_name(B.make_desc(64, 128, 56, 56, 3, 1, 1), -1) == "invalid"
 
 

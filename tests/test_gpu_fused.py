@@ -123,3 +123,103 @@ def test_epilogue_matches_unfused_sequence(dtype):
     want = th.clamp(y0.float() * sc + sh, 0.0, 6.0)
     tol = 1e-5 if dtype == "f32" else 3e-2
     assert th.allclose(y.float(), want, rtol=tol, atol=tol)
+
+
+# ------------------------------------------------------- channels-last forward
+# (layer, out_c_offset, out_c_total, activation, expected kernel)
+NHWC_CASES = [
+    (WL.Layer(N=2, C=64, H=29, W=29, k=3, s=1, p=1, bias=True), 0, 0, "relu6", "nhwc"),
+    (WL.Layer(N=3, C=72, H=33, W=33, k=3, s=2, p=1, dtype="bf16"), 0, 0, "relu", "nhwc"),
+    (WL.Layer(N=2, C=40, H=21, W=26, k=5, s=1, p=2, bias=True, dtype="f16"), 0, 0, "none", "nhwc"),
+    (WL.Layer(N=2, C=36, H=30, W=31, k=7, s=2, p=3), 0, 0, "relu", "nhwc"),
+    (WL.Layer(N=1, C=32, H=56, W=56, k=7, s=1, p=3, dtype="bf16"), 0, 0, "relu6", "nhwc"),
+    (WL.Layer(N=2, C=16, H=14, W=14, k=5, s=2, p=2, dtype="f16"), 0, 0, "none", "nhwc"),
+    (WL.Layer(N=2, C=32, H=17, W=17, k=3, s=1, p=0), 4, 40, "relu", "nhwc"),      # 16-byte-aligned slice
+    (WL.Layer(N=2, C=32, H=17, W=17, k=3, s=1, p=1, dtype="bf16"), 1, 35, "none", "nhwc"),  # unaligned slice
+    (WL.Layer(N=2, C=6, H=15, W=15, k=3, s=1, p=1), 0, 0, "relu", "generic"),     # C*4 not a multiple of 16
+    (WL.Layer(N=2, C=8, H=12, W=12, k=3, s=1, p=1, m=2, bias=True, dtype="f16"), 2, 20, "relu6", "generic"),
+    (WL.Layer(N=2, C=16, H=19, W=19, k=3, s=1, p=2, d=2), 0, 0, "none", "generic"),
+    (WL.Layer(N=2, C=16, H=16, W=16, k=9, s=1, p=4), 0, 0, "none", "generic"),
+]
+NHWC_IDS = ["k3s1_f32", "k3s2_bf16_chtail", "k5s1_f16", "k7s2_f32", "k7s1_bf16_56", "k5s2_f16_small",
+            "slice_aligned", "slice_unaligned", "C6_generic", "m2_generic", "d2_generic", "k9_generic"]
+
+
+def nhwc_inputs(L, seed=0):
+    inp = WL.make_inputs(L, seed)
+    x = to_dev(inp.x).permute(0, 2, 3, 1).contiguous()
+    return inp, x
+
+
+def nhwc_run(L, off, ctot, act, x, inp, scale=None, shift=None):
+    th = torch()
+    d = B.make_desc(**L.desc_kwargs(), out_c_offset=off, out_c_total=ctot)
+    y = empty_dev((L.N, L.Ho, L.Wo, ctot or L.OC), L.dtype, fill=-9.0)
+    B.dwconv2d_fwd_nhwc(d, x, to_dev(inp.w), to_dev(inp.b) if inp.b is not None else None, y,
+                        scale=None if scale is None else to_dev(scale),
+                        shift=None if shift is None else to_dev(shift), act=act)
+    th.cuda.synchronize()
+    return d, np.ascontiguousarray(to_f64(y).transpose(0, 3, 1, 2))
+
+
+@pytest.mark.parametrize("L,off,ctot,act,family", NHWC_CASES, ids=NHWC_IDS)
+def test_nhwc_vs_oracle(L, off, ctot, act, family):
+    inp, x = nhwc_inputs(L)
+    scale, shift = folded_bn(L.OC, L.dtype, seed=1) if act != "none" else (None, None)
+    d, got = nhwc_run(L, off, ctot, act, x, inp, scale, shift)
+    assert B.dwconv2d_plan_name(d, 4) == family
+    cv = oconv(L, off=off, c_total=ctot or None)
+    ref = np.full(got.shape, -9.0)
+    oracle.fwd_epilogue(cv, inp.x.f64, inp.w.f64, None if inp.b is None else inp.b.f64,
+                        None if scale is None else scale.f64, None if shift is None else shift.f64,
+                        act, y=ref)
+    assert_close(got, ref, L.dtype, L.k * L.k, f"nhwc {L.label()}")
+    if ctot:
+        assert np.all(got[:, :off] == -9.0) and np.all(got[:, off + L.OC:] == -9.0)
+
+
+def test_nhwc_misaligned_input_takes_generic_kernel():
+    """An x that is not 16-byte aligned cannot be a tensor-map base: the call
+    runs on the generic kernel and gives the same values."""
+    th = torch()
+    L = WL.Layer(N=2, C=32, H=20, W=20, k=3, s=1, p=1)
+    inp, x = nhwc_inputs(L)
+    buf = th.empty(x.numel() + 1, dtype=x.dtype, device="cuda")
+    xs = buf[1:].view(x.shape)
+    xs.copy_(x)
+    _, got = nhwc_run(L, 0, 0, "none", xs, inp)
+    _, ref = nhwc_run(L, 0, 0, "none", x, inp)
+    assert_close(got, ref, L.dtype, 9, "misaligned nhwc")
+    assert_close(got, oracle.fwd(oconv(L), inp.x.f64, inp.w.f64), L.dtype, 9, "misaligned nhwc vs oracle")
+
+
+def test_nhwc_matches_nchw_forward_bitwise_where_sums_agree():
+    """A delta filter makes every output one product, so the channels-last
+    and NCHW kernels must agree bit for bit (a check of the layout mapping,
+    independent of summation order)."""
+    th = torch()
+    L = WL.Layer(N=2, C=64, H=23, W=23, k=5, s=2, p=2, dtype="bf16")
+    inp, x = nhwc_inputs(L)
+    w = np.zeros((L.OC, 5, 5))
+    w[:, 1, 3] = np.linspace(0.5, 2.0, L.OC)
+    wt = synth.Tensor(w, w.shape, "bf16")
+    inp.w = wt
+    d, got = nhwc_run(L, 0, 0, "none", x, inp)
+    y = empty_dev((L.N, L.OC, L.Ho, L.Wo), "bf16")
+    B.dwconv2d_fwd(d, to_dev(inp.x), to_dev(wt), None, y)
+    th.cuda.synchronize()
+    assert np.array_equal(got, to_f64(y))
+
+
+def test_nhwc_full_size_mobilenet_layer_sampled():
+    """A full-size MobileNet layer in channels-last form (64 x 128 x 56 x 56
+    fp32, 3x3 stride 1), compared with the oracle on sampled samples and
+    channels."""
+    L = WL.Layer(N=64, C=128, H=56, W=56, k=3, s=1, p=1)
+    inp, x = nhwc_inputs(L)
+    d, got = nhwc_run(L, 0, 0, "none", x, inp)
+    assert B.dwconv2d_plan_name(d, 4) == "nhwc"
+    nsel, csel = [0, 31, 63], [0, 37, 127]
+    cv = oconv(L, N=len(nsel), C=len(csel))
+    ref = oracle.fwd(cv, inp.x.f64[np.ix_(nsel, csel)], inp.w.f64[csel])
+    assert_close(got[np.ix_(nsel, csel)], ref, "f32", 9, "mobilenet nhwc")
