@@ -35,7 +35,10 @@ struct NCfg {
   int bh, bw;            // input box rows / columns
   int cg;                // channels per unit (128 bytes)
   int tiles_h, tiles_w, groups;
-  int64_t units;
+  int64_t units;         // below 2^31
+  FastDiv d_per_n;       // units per sample: tiles_h * tiles_w * groups
+  FastDiv d_tpr;         // units per tile row: tiles_w * groups
+  FastDiv d_groups;
   int box_bytes;         // bh * bw * 128
   int stage_bytes;       // box, rounded up to 128 bytes
   int tab_floats;        // K*K*cg taps + bias, scale, shift (cg each)
@@ -103,8 +106,13 @@ __device__ __forceinline__ uint4 pack16<__nv_bfloat16>(const float* a) {
   return make_uint4(v[0], v[1], v[2], v[3]);
 }
 
+// Resident CTAs the register budget is sized for: three where 80 registers
+// hold the block without spilling (fp32, or stride 2), else two.
+template <typename T, int S>
+constexpr int min_ctas() { return (sizeof(T) == 4 || S == 2) ? 3 : 2; }
+
 template <typename T, int K, int S, int PX>
-__global__ void __launch_bounds__(kNT, 2)
+__global__ void __launch_bounds__(kNT, (min_ctas<T, S>()))
 tiled_kernel(Conv c, NCfg g, const __grid_constant__ CUtensorMap tmap, unsigned int* timeouts,
              const T* __restrict__ w, const T* __restrict__ bias, T* __restrict__ y, Epi ep) {
   constexpr int VEC = Vec<T>::n;
@@ -127,18 +135,16 @@ tiled_kernel(Conv c, NCfg g, const __grid_constant__ CUtensorMap tmap, unsigned 
   const int spr = g.tw / PX;            // strips per tile row
   const int sr = strip / spr, sc = strip - sr * spr;
   const bool strip_on = strip < g.th * spr;
-  const int64_t per_n = (int64_t)g.tiles_h * g.tiles_w * g.groups;
 
   auto coords = [&](int64_t u, int& n, int& oh0, int& ow0, int& c0) {
-    n = (int)(u / per_n);
-    int64_t r = u - (int64_t)n * per_n;
-    const int tpr = g.tiles_w * g.groups;
-    const int thi = (int)(r / tpr);
-    r -= (int64_t)thi * tpr;
-    const int twi = (int)(r / g.groups);
-    c0 = (int)(r - (int64_t)twi * g.groups) * g.cg;
-    oh0 = thi * g.th;
-    ow0 = twi * g.tw;
+    uint32_t q, thi, twi;
+    uint32_t r = g.d_per_n.divmod((uint32_t)u, q);
+    n = (int)q;
+    r = g.d_tpr.divmod(r, thi);
+    r = g.d_groups.divmod(r, twi);
+    c0 = (int)r * g.cg;
+    oh0 = (int)thi * g.th;
+    ow0 = (int)twi * g.tw;
   };
   auto issue = [&](int64_t u, unsigned char* box, float* tab, uint64_t* bar) {
     int n, oh0, ow0, c0;
@@ -302,6 +308,10 @@ bool plan_tiled(const Conv& c, int px, NCfg* out) {
     g.tiles_w = (int)((c.Wo + g.tw - 1) / g.tw);
     g.groups = (int)((c.C + g.cg - 1) / g.cg);
     g.units = (int64_t)c.N * g.tiles_h * g.tiles_w * g.groups;
+    if (g.units >= (int64_t(1) << 31)) continue;
+    g.d_per_n = FastDiv((uint32_t)g.tiles_h * g.tiles_w * g.groups);
+    g.d_tpr = FastDiv((uint32_t)g.tiles_w * g.groups);
+    g.d_groups = FastDiv((uint32_t)g.groups);
     g.box_bytes = g.bh * g.bw * 128;
     g.stage_bytes = (g.box_bytes + 127) / 128 * 128;
     g.tab_floats = (c.kh * c.kw + 3) * g.cg;

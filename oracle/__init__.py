@@ -6,8 +6,9 @@ package, and this package never imports the product. It shares no code with
 the CUDA library.
 
 The arithmetic lives in ``dwconv_oracle.c`` (direct nested loops over the
-definition of forward, bwd_data and bwd_weight, and the per-channel epilogue
-of the fused forward). This module only compiles it
+definition of forward, bwd_data and bwd_weight, the per-channel epilogue of
+the fused forward, and the pointwise 1x1 step of a depthwise-separable
+block). This module only compiles it
 with gcc, marshals numpy float64 arrays to it, and expresses the fused
 multi-branch calls the way the DynamicConvolutionOperator README describes
 them ("Solution": one output per dilation branch, each stored into its own
@@ -122,6 +123,8 @@ def _load():
         lib.oracle_dwconv2d_bwd_data.argtypes = [P, dp, dp, dp]
         lib.oracle_dwconv2d_bwd_weight.argtypes = [P, dp, dp, dp, dp]
         lib.oracle_epilogue.argtypes = [P, dp, dp, ctypes.c_int, dp]
+        i64 = ctypes.c_int64
+        lib.oracle_pointwise.argtypes = [i64, i64, i64, i64, dp, dp, dp]
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -171,6 +174,31 @@ def fwd_epilogue(cv: Conv, x, w, bias=None, scale=None, shift=None, act="none", 
     sh = None if shift is None else _f64(shift, (cv.OC,))
     d = cv._c()
     _load().oracle_epilogue(ctypes.byref(d), _ptr(sc), _ptr(sh), ACTS[act], _ptr(y))
+    return y
+
+
+def separable(cv: Conv, x, w_dw, dw_scale=None, dw_shift=None, dw_act="none", w_pw=None,
+              pw_scale=None, pw_shift=None, pw_act="none"):
+    """Depthwise-separable block: z = act1(scale1 * dwconv(x) + shift1) over
+    all C*m depthwise channels, then y = act2(scale2 * (w_pw @ z) + shift2)
+    with w_pw [cout, C*m]. Returns y [N, cout, Ho, Wo] (cv's slice fields
+    are ignored: z is the full C*m channels)."""
+    lib = _load()
+    dcv = Conv(N=cv.N, C=cv.C, H=cv.H, W=cv.W, kh=cv.kh, kw=cv.kw, sh=cv.sh, sw=cv.sw, ph=cv.ph, pw=cv.pw,
+               dh=cv.dh, dw=cv.dw, m=cv.m)
+    z = fwd_epilogue(dcv, x, w_dw, None, dw_scale, dw_shift, dw_act)
+    cin = dcv.OC
+    wp = np.ascontiguousarray(np.asarray(w_pw, dtype=np.float64))
+    cout = wp.shape[0]
+    assert wp.shape == (cout, cin)
+    hw = dcv.Ho * dcv.Wo
+    y = np.empty((cv.N, cout, dcv.Ho, dcv.Wo), dtype=np.float64)
+    lib.oracle_pointwise(cv.N, cin, cout, hw, _ptr(z), _ptr(wp), _ptr(y))
+    pcv = Conv(N=cv.N, C=cout, H=dcv.Ho, W=dcv.Wo, kh=1, kw=1)
+    sc = None if pw_scale is None else _f64(pw_scale, (cout,))
+    sh = None if pw_shift is None else _f64(pw_shift, (cout,))
+    pd = pcv._c()
+    lib.oracle_epilogue(ctypes.byref(pd), _ptr(sc), _ptr(sh), ACTS[pw_act], _ptr(y))
     return y
 
 

@@ -34,6 +34,8 @@
  *               (the grad-weight kernel and grad_bias of #3057).
  *   epilogue    y = act(scale * y + shift) per output channel after the
  *               forward (oracle_epilogue below).
+ *   pointwise   the 1x1 convolution that follows the depthwise layer in a
+ *               depthwise-separable block (oracle_pointwise below).
  *
  * Readings where the pages are silent: cross-correlation (no kernel flip, as
  * PyTorch's conv2d); Ho = floor((H + 2ph - dh(kh-1) - 1)/sh) + 1; symmetric
@@ -192,6 +194,27 @@ void oracle_epilogue(const oracle_desc* d, const double* scale, const double* sh
         if (act == 2) v = v < 6.0 ? v : 6.0;
         yp[i] = v;
       }
+    }
+  }
+}
+
+/* Pointwise (1x1) convolution of a depthwise-separable block:
+ *   y[n, co, i] = sum_{ci < cin} wp[co, ci] * z[n, ci, i]     (i over hw pixels)
+ * z [n][cin][hw], wp [cout][cin] (PyTorch's [cout, cin, 1, 1]), y
+ * [n][cout][hw], overwritten. Source: "Spatial Depthwise Convolution on the
+ * GPU #3057", the MobileNet benchmark table that times the 1x1 layer after
+ * each depthwise layer. */
+void oracle_pointwise(int64_t n, int64_t cin, int64_t cout, int64_t hw, const double* z,
+                      const double* wp, double* y) {
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < n * cout; ++t) {
+    const int64_t b = t / cout, co = t % cout;
+    double* yp = y + (b * cout + co) * hw;
+    for (int64_t i = 0; i < hw; ++i) yp[i] = 0.0;
+    for (int64_t ci = 0; ci < cin; ++ci) {
+      const double wv = wp[co * cin + ci];
+      const double* zp = z + (b * cin + ci) * hw;
+      for (int64_t i = 0; i < hw; ++i) yp[i] += wv * zp[i];
     }
   }
 }

@@ -37,6 +37,9 @@ MUTANTS = {
     "epi_relu6_uncapped": ("if (act == 2) v = v < 6.0 ? v : 6.0;", ""),
     "epi_scale_by_input_channel": ("const double sc = scale ? scale[oc] : 1.0;",
                                    "const double sc = scale ? scale[oc / d->m] : 1.0;"),
+    "pw_weight_transposed": ("const double wv = wp[co * cin + ci];", "const double wv = wp[ci * cout + co];"),
+    "pw_channel_dropped": ("for (int64_t ci = 0; ci < cin; ++ci) {\n      const double wv",
+                           "for (int64_t ci = 1; ci < cin; ++ci) {\n      const double wv"),
     "bias_grad_short": ("for (int64_t i = 0; i < Ho * Wo; ++i) acc += gyp[i];",
                         "for (int64_t i = 1; i < Ho * Wo; ++i) acc += gyp[i];"),
 }

@@ -342,3 +342,56 @@ def test_epilogue_identity_and_activation_cases():
     sc = 2.0 ** np.arange(cv.OC)
     ys = oracle.fwd_epilogue(cv, x, w, scale=sc)
     assert np.array_equal(ys[:, 1:1 + cv.OC], y0[:, 1:1 + cv.OC] * sc[None, :, None, None])
+
+
+# ---- depthwise-separable block ----------------------------------------------
+
+@pytest.mark.parametrize("cv,cout", [(Conv(N=2, C=6, H=9, W=8, kh=3, kw=3, ph=1, pw=1), 10),
+                                     (Conv(N=1, C=4, H=11, W=11, kh=3, kw=3, sh=2, sw=2, ph=1, pw=1), 3),
+                                     (Conv(N=2, C=3, H=8, W=7, kh=5, kw=5, ph=2, pw=2, m=2), 5)],
+                         ids=["s1", "s2", "k5m2"])
+def test_separable_block_is_torch_sequence(cv, cout):
+    """The block equals torch's float64 depthwise conv2d -> batch_norm(eval)
+    -> ReLU6 -> 1x1 conv2d -> batch_norm(eval) -> ReLU on the same values."""
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    rng = np.random.default_rng(cv.C * 10 + cout)
+    x = 3.0 * rng.standard_normal((cv.N, cv.C, cv.H, cv.W))
+    wd, wp = rng.standard_normal((cv.OC, cv.kh, cv.kw)), rng.standard_normal((cout, cv.OC))
+    bn = lambda c: (rng.standard_normal(c), rng.standard_normal(c), rng.standard_normal(c),
+                    rng.uniform(0.5, 2.0, c))
+    g1, b1, m1, v1 = bn(cv.OC)
+    g2, b2, m2, v2 = bn(cout)
+    eps = 1e-5
+    s1 = g1 / np.sqrt(v1 + eps)
+    s2 = g2 / np.sqrt(v2 + eps)
+    T = torch.tensor
+    z = F.conv2d(T(x), T(wd.reshape(cv.OC, 1, cv.kh, cv.kw)), stride=(cv.sh, cv.sw), padding=(cv.ph, cv.pw),
+                 dilation=(cv.dh, cv.dw), groups=cv.C)
+    z = F.hardtanh(F.batch_norm(z, T(m1), T(v1), T(g1), T(b1), training=False, eps=eps), 0.0, 6.0)
+    y = F.conv2d(z, T(wp.reshape(cout, cv.OC, 1, 1)))
+    y = F.relu(F.batch_norm(y, T(m2), T(v2), T(g2), T(b2), training=False, eps=eps))
+    got = oracle.separable(cv, x, wd, s1, b1 - m1 * s1, "relu6", wp, s2, b2 - m2 * s2, "relu")
+    np.testing.assert_allclose(got, y.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_separable_block_special_cases():
+    """Identity pointwise weights give the depthwise stage unchanged (bit for
+    bit); a row of ones sums the channels exactly (dyadic values); a
+    permutation moves whole channels."""
+    cv = Conv(N=2, C=5, H=7, W=6, kh=3, kw=3, ph=1, pw=1)
+    x = np.round(RNG.standard_normal((cv.N, cv.C, cv.H, cv.W)) * 64) / 64
+    wd = np.round(RNG.standard_normal((cv.C, 3, 3)) * 16) / 16
+    z = oracle.fwd_epilogue(cv, x, wd, act="relu")
+    assert np.array_equal(oracle.separable(cv, x, wd, dw_act="relu", w_pw=np.eye(cv.C)), z)
+    ones = np.ones((1, cv.C))
+    assert np.array_equal(oracle.separable(cv, x, wd, dw_act="relu", w_pw=ones)[:, 0], z.sum(axis=1))
+    perm = np.eye(cv.C)[[3, 0, 4, 1, 2]]
+    assert np.array_equal(oracle.separable(cv, x, wd, w_pw=perm), oracle.fwd(cv, x, wd)[:, [3, 0, 4, 1, 2]])
+    # the second epilogue acts per output channel of the pointwise step
+    sc = np.array([2.0, -1.0])
+    y = oracle.separable(cv, x, wd, w_pw=np.vstack([ones, ones]), pw_scale=sc, pw_shift=np.array([0.5, 0.25]),
+                         pw_act="relu")
+    s = oracle.fwd(cv, x, wd).sum(axis=1)
+    assert np.array_equal(y[:, 0], np.maximum(2.0 * s + 0.5, 0.0))
+    assert np.array_equal(y[:, 1], np.maximum(-s + 0.25, 0.0))
