@@ -25,7 +25,7 @@ SYMBOLS = ("dwconv2d_output_shape", "dwconv2d_fwd", "dwconv2d_bwd_data",
            "dwconv2d_bwd_data_multi", "dwconv_status_string", "dwconv2d_plan_name",
            "dwconv2d_multi_plan_name", "dwconv_fma_probe", "dwconv2d_bwd_weight_noalloc",
            "dwconv_device_timeouts", "dwconv_wait_selftest", "dwconv2d_fwd_epilogue",
-           "dwconv2d_fwd_nhwc")
+           "dwconv2d_fwd_nhwc", "dwconv2d_separable_nhwc", "dwconv2d_separable_plan_name")
 
 # dwconv_act_t
 ACTS = {"none": 0, "relu": 1, "relu6": 2}
@@ -88,6 +88,10 @@ def load():
     lib.dwconv2d_fwd.argtypes = [P, vp, vp, vp, vp, vp]
     lib.dwconv2d_fwd_epilogue.argtypes = [P, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp]
     lib.dwconv2d_fwd_nhwc.argtypes = [P, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp]
+    lib.dwconv2d_separable_nhwc.argtypes = [P, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int64, vp, vp, vp,
+                                            ctypes.c_int, vp, vp]
+    lib.dwconv2d_separable_plan_name.argtypes = [P, ctypes.c_int64]
+    lib.dwconv2d_separable_plan_name.restype = ctypes.c_char_p
     lib.dwconv2d_bwd_data.argtypes = [P, vp, vp, vp, ctypes.c_int, vp]
     lib.dwconv2d_bwd_weight_workspace_size.argtypes = [P]
     lib.dwconv2d_bwd_weight_workspace_size.restype = ctypes.c_size_t
@@ -106,7 +110,7 @@ def load():
     lib.dwconv_wait_selftest.argtypes = [ctypes.c_uint, vp]
     for name in SYMBOLS:
         if name not in ("dwconv2d_bwd_weight_workspace_size", "dwconv_status_string", "dwconv2d_plan_name",
-                        "dwconv2d_multi_plan_name"):
+                        "dwconv2d_multi_plan_name", "dwconv2d_separable_plan_name"):
             getattr(lib, name).restype = st
     _lib = lib
     return lib
@@ -164,6 +168,21 @@ def dwconv2d_fwd_nhwc(desc: Desc, x, w, bias, y, scale=None, shift=None, act=0, 
     _check(load().dwconv2d_fwd_nhwc(ctypes.byref(desc), _ptr(x), _ptr(w), _ptr(bias), _ptr(scale),
                                      _ptr(shift), a, _ptr(y), _stream(stream)),
            "dwconv2d_fwd_nhwc")
+
+
+def dwconv2d_separable_nhwc(desc: Desc, x, w_dw, cout: int, w_pw, y, dw_scale=None, dw_shift=None,
+                            dw_act=0, pw_scale=None, pw_shift=None, pw_act=0, stream=None):
+    """Depthwise-separable block; x [N, H, W, C], y [N, Ho, Wo, out_c_total]."""
+    a1 = ACTS[dw_act] if isinstance(dw_act, str) else int(dw_act)
+    a2 = ACTS[pw_act] if isinstance(pw_act, str) else int(pw_act)
+    _check(load().dwconv2d_separable_nhwc(ctypes.byref(desc), _ptr(x), _ptr(w_dw), _ptr(dw_scale),
+                                           _ptr(dw_shift), a1, int(cout), _ptr(w_pw), _ptr(pw_scale),
+                                           _ptr(pw_shift), a2, _ptr(y), _stream(stream)),
+           "dwconv2d_separable_nhwc")
+
+
+def dwconv2d_separable_plan_name(desc: Desc, cout: int) -> str:
+    return load().dwconv2d_separable_plan_name(ctypes.byref(desc), int(cout)).decode()
 
 
 def dwconv2d_bwd_data(desc: Desc, gy, w, gx, accumulate=0, stream=None):

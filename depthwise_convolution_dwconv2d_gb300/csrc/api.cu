@@ -68,6 +68,8 @@ dwconv_status_t check_ptr(const void* p, int es, bool required) {
   return aligned(p, es) ? DWCONV_OK : DWCONV_ERR_MISALIGNED;
 }
 
+bool act_ok(int a) { return a == DWCONV_ACT_NONE || a == DWCONV_ACT_RELU || a == DWCONV_ACT_RELU6; }
+
 #define DW_TRY(expr)                          \
   do {                                        \
     dwconv_status_t st__ = (expr);            \
@@ -162,8 +164,7 @@ dwconv_status_t dwconv2d_fwd_epilogue(const dwconv2d_desc_t* desc, const void* x
                                       int act, void* y, cudaStream_t stream) {
   Conv c;
   DW_TRY(make_conv(desc, &c));
-  if (act != DWCONV_ACT_NONE && act != DWCONV_ACT_RELU && act != DWCONV_ACT_RELU6)
-    return DWCONV_ERR_INVALID_ARG;
+  if (!act_ok(act)) return DWCONV_ERR_INVALID_ARG;
   const int es = esize(c.dtype);
   DW_TRY(check_ptr(w, es, true));
   DW_TRY(check_ptr(bias, es, false));
@@ -181,8 +182,7 @@ dwconv_status_t dwconv2d_fwd_nhwc(const dwconv2d_desc_t* desc, const void* x, co
                                   void* y, cudaStream_t stream) {
   Conv c;
   DW_TRY(make_conv(desc, &c));
-  if (act != DWCONV_ACT_NONE && act != DWCONV_ACT_RELU && act != DWCONV_ACT_RELU6)
-    return DWCONV_ERR_INVALID_ARG;
+  if (!act_ok(act)) return DWCONV_ERR_INVALID_ARG;
   const int es = esize(c.dtype);
   DW_TRY(check_ptr(w, es, true));
   DW_TRY(check_ptr(bias, es, false));
@@ -192,6 +192,57 @@ dwconv_status_t dwconv2d_fwd_nhwc(const dwconv2d_desc_t* desc, const void* x, co
   DW_TRY(check_ptr(x, es, true));
   DW_TRY(check_ptr(y, es, true));
   return cuda_status(nhwc::fwd(c, x, w, bias, y, stream, Epi{scale, shift, act}));
+}
+
+namespace {
+
+// The separable block's descriptor: its slice fields describe y's channels
+// (cout of them), not the depthwise layer's C*m.
+dwconv_status_t make_sep(const dwconv2d_desc_t* desc, int64_t cout, Conv* c, int64_t* ctot, int64_t* off) {
+  if (!desc) return DWCONV_ERR_INVALID_ARG;
+  dwconv2d_desc_t d = *desc;
+  d.out_c_offset = 0;
+  d.out_c_total = 0;
+  DW_TRY(make_conv(&d, c));
+  if (cout < 1) return DWCONV_ERR_INVALID_ARG;
+  if (cout > (int64_t(1) << 20)) return DWCONV_ERR_UNSUPPORTED;
+  *off = desc->out_c_offset;
+  *ctot = desc->out_c_total == 0 ? cout : desc->out_c_total;
+  if (*off < 0 || *ctot < 1 || *off + cout > *ctot) return DWCONV_ERR_INVALID_ARG;
+  if (c->N > 0 && c->N > kMaxElems / (*ctot * c->Ho * c->Wo)) return DWCONV_ERR_UNSUPPORTED;
+  if (!sep::supported(*c)) return DWCONV_ERR_UNSUPPORTED;
+  return DWCONV_OK;
+}
+
+}  // namespace
+
+dwconv_status_t dwconv2d_separable_nhwc(const dwconv2d_desc_t* desc, const void* x, const void* w_dw,
+                                        const void* dw_scale, const void* dw_shift, int dw_act, int64_t cout,
+                                        const void* w_pw, const void* pw_scale, const void* pw_shift,
+                                        int pw_act, void* y, cudaStream_t stream) {
+  Conv c;
+  int64_t ctot = 0, off = 0;
+  DW_TRY(make_sep(desc, cout, &c, &ctot, &off));
+  if (!act_ok(dw_act) || !act_ok(pw_act)) return DWCONV_ERR_INVALID_ARG;
+  const int es = esize(c.dtype);
+  DW_TRY(check_ptr(w_dw, es, true));
+  DW_TRY(check_ptr(w_pw, es, true));
+  DW_TRY(check_ptr(dw_scale, es, false));
+  DW_TRY(check_ptr(dw_shift, es, false));
+  DW_TRY(check_ptr(pw_scale, es, false));
+  DW_TRY(check_ptr(pw_shift, es, false));
+  if (c.N == 0) return DWCONV_OK;
+  DW_TRY(check_ptr(x, es, true));
+  DW_TRY(check_ptr(y, es, true));
+  return cuda_status(sep::run(c, cout, ctot, off, x, w_dw, dw_scale, dw_shift, dw_act, w_pw, pw_scale, pw_shift,
+                              pw_act, y, stream));
+}
+
+const char* dwconv2d_separable_plan_name(const dwconv2d_desc_t* desc, int64_t cout) {
+  Conv c;
+  int64_t ctot = 0, off = 0;
+  if (make_sep(desc, cout, &c, &ctot, &off) != DWCONV_OK) return "invalid";
+  return algo_name(sep::plan(c, cout));
 }
 
 dwconv_status_t dwconv2d_bwd_data(const dwconv2d_desc_t* desc, const void* gy, const void* w,

@@ -20,4 +20,20 @@ cudaError_t fwd(const Conv& c, const void* x, const void* w, const void* b, void
                 const Epi& ep);
 
 }  // namespace nhwc
+
+// Depthwise-separable block, channels-last (separable.cu).
+namespace sep {
+
+// The generic kernel can stage the depthwise result of one pixel (C*m fp32
+// values in at most 96 KB of shared memory).
+bool supported(const Conv& c);
+// Algo::SepTc for the tensor-core kernel, Algo::Generic otherwise.
+Algo plan(const Conv& c, int64_t cout);
+// x [N, H, W, C]; wd [C*m, kh, kw]; wp [cout, C*m]; y [N, Ho, Wo, ctot]
+// (channels [off, off + cout) written).
+cudaError_t run(const Conv& c, int64_t cout, int64_t ctot, int64_t off, const void* x, const void* wd,
+                const void* s1, const void* h1, int a1, const void* wp, const void* s2, const void* h2, int a2,
+                void* y, cudaStream_t s);
+
+}  // namespace sep
 }  // namespace dwconv

@@ -33,6 +33,7 @@ const char* algo_name(Algo a) {
     case Algo::Plane: return "plane";
     case Algo::TcWgrad: return "tcwgrad";
     case Algo::Nhwc: return "nhwc";
+    case Algo::SepTc: return "septc";
   }
   return "unknown";
 }

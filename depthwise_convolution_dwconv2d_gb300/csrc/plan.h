@@ -15,6 +15,7 @@ enum class Algo {
   Plane = 4,     // plane.cu: 3x3 on small planes, one warp per group of whole planes
   TcWgrad = 5,   // wgrad_tc.cu: large-kernel weight gradient on tcgen05 (fp16 / bf16)
   Nhwc = 6,      // nhwc.cu: channels-last forward, TMA-staged channel-vector tiles
+  SepTc = 7,     // separable.cu: depthwise + pointwise block, pointwise on tcgen05 (fp16 / bf16)
 };
 
 struct WPlan {

@@ -17,8 +17,9 @@ oracle, which widens them exactly to float64, so quantisation of the inputs is
 never counted as error.
 
 Stream ids (per tensor, so shapes can change without reshuffling others):
-x = 0, w = 1, bias = 2, gy = 3, epilogue scale = 4, epilogue shift = 5;
-branch i > 0 of a multi-branch op uses w = 1 + 16 i and bias = 2 + 16 i.
+x = 0, w = 1, bias = 2, gy = 3, epilogue scale = 4, epilogue shift = 5,
+pointwise weights / scale / shift = 6 / 7 / 8; branch i > 0 of a
+multi-branch op uses w = 1 + 16 i and bias = 2 + 16 i.
 """
 from __future__ import annotations
 
@@ -32,6 +33,7 @@ _M2 = np.uint64(0x94D049BB133111EB)
 
 STREAM_X, STREAM_W, STREAM_B, STREAM_GY = 0, 1, 2, 3
 STREAM_SCALE, STREAM_SHIFT = 4, 5
+STREAM_PW, STREAM_PW_SCALE, STREAM_PW_SHIFT = 6, 7, 8
 
 _CHUNK = 1 << 22
 

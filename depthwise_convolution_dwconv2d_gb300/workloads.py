@@ -166,6 +166,13 @@ def make_scale_shift(L: Layer, seed: int = 0):
             synth.normal_tensor((L.OC,), L.dtype, seed, synth.STREAM_SHIFT, std=0.5))
 
 
+def make_pointwise(L: Layer, cout: int, seed: int = 0):
+    """1x1 weights [cout, C*m] ~ N(0, 1/(C*m)), scale ~ U[0.5, 1.5], shift ~ N(0, 0.25)."""
+    return (synth.normal_tensor((cout, L.OC), L.dtype, seed, synth.STREAM_PW, std=1.0 / math.sqrt(L.OC)),
+            synth.uniform_tensor((cout,), L.dtype, seed, synth.STREAM_PW_SCALE, lo=0.5, hi=1.5),
+            synth.normal_tensor((cout,), L.dtype, seed, synth.STREAM_PW_SHIFT, std=0.5))
+
+
 def make_inputs(L: Layer, seed: int = 0, branch: int = 0, gy_channels: int | None = None) -> Inputs:
     """x, w, bias and grad_out for one layer, drawn as the module docstring says."""
     return Inputs(make_x(L, seed), make_w(L, seed, branch), make_b(L, seed, branch) if L.bias else None,

@@ -201,6 +201,33 @@ dwconv_status_t dwconv2d_fwd_nhwc(const dwconv2d_desc_t* desc, const void* x, co
                                   const void* bias, const void* scale, const void* shift, int act,
                                   void* y, cudaStream_t stream);
 
+/* Depthwise-separable block, channels-last: the depthwise layer of desc,
+ * its epilogue, then a 1x1 (pointwise) convolution to cout channels and its
+ * epilogue, in one call:
+ *   z[n, h, w, k]  = dw_act(dw_scale[k] * dwconv(x)[n, h, w, k] + dw_shift[k])
+ *                    for the k < C*m depthwise channels (no bias: fold it
+ *                    into dw_shift), rounded to desc->dtype
+ *   y[n, h, w, off + o] = pw_act(pw_scale[o] * sum_k w_pw[o, k] z[n, h, w, k]
+ *                                + pw_shift[o])       for o < cout
+ * with fp32 accumulation in both stages. x [N, H, W, C] and y [N, Ho, Wo,
+ * out_c_total] are channels-last; w_dw [C*m, kh, kw]; w_pw [cout, C*m]
+ * (PyTorch's [cout, C*m, 1, 1]); dw_scale / dw_shift have C*m values,
+ * pw_scale / pw_shift cout values, each NULL for 1 / 0; the acts are
+ * dwconv_act_t values. desc->out_c_offset / out_c_total describe y's channel
+ * axis (0 / 0: y has exactly cout channels); z never reaches memory.
+ * (Source: the MobileNet table of "Spatial Depthwise Convolution on the GPU
+ * #3057", which times each depthwise layer with the 1x1 layer after it.)
+ * fp16 / bf16 blocks with a 3x3 or 5x5 filter, equal strides of 1 or 2,
+ * dilation 1, one filter per channel and C a multiple of 64 (x and w_pw
+ * 16-byte aligned) run the pointwise step on the tensor cores; every other
+ * block runs on a generic kernel (DWCONV_ERR_UNSUPPORTED when C*m fp32
+ * values of one pixel exceed 96 KB). Errors as dwconv2d_fwd_epilogue;
+ * cout < 1 or a y slice past out_c_total is DWCONV_ERR_INVALID_ARG. */
+dwconv_status_t dwconv2d_separable_nhwc(const dwconv2d_desc_t* desc, const void* x, const void* w_dw,
+                                        const void* dw_scale, const void* dw_shift, int dw_act, int64_t cout,
+                                        const void* w_pw, const void* pw_scale, const void* pw_shift,
+                                        int pw_act, void* y, cudaStream_t stream);
+
 /* Fused multi-branch forward (the DynamicConvolutionOperator's single launch
  * for dilation 1, 3, 5 whose results are stored straight into slices of one
  * concatenated tensor): nbranch (1..8) descriptors over the same x. All
@@ -236,6 +263,10 @@ const char* dwconv_status_string(dwconv_status_t status);
  * An "ibgemm" pass whose input pointer (a "tcwgrad" pass whose x or grad_out
  * pointer) is not 16-byte aligned runs on the direct kernels instead. */
 const char* dwconv2d_plan_name(const dwconv2d_desc_t* desc, int pass);
+
+/* Kernel family of dwconv2d_separable_nhwc for this block: "septc" (the
+ * fused tensor-core kernel), "generic" or "invalid". Host only. */
+const char* dwconv2d_separable_plan_name(const dwconv2d_desc_t* desc, int64_t cout);
 
 /* Kernel family used by dwconv2d_fwd_multi / dwconv2d_bwd_data_multi for
  * these branches ("tile" = the fused single-launch kernels, "generic" = the

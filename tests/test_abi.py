@@ -151,6 +151,34 @@ def test_nhwc_argument_checks_and_routing(lib):
     assert B.dwconv2d_plan_name(B.make_desc(8, 32, 30, 30, 9, 1, 4), 4) == "generic"
 
 
+def test_separable_argument_checks_and_routing(lib):
+    d = B.make_desc(2, 64, 8, 8, 3, 1, 1, dtype="bf16")
+    fn = B.dwconv2d_separable_nhwc
+    assert status_of(fn, d, P, P, 0, P, P) == INVALID                       # cout < 1
+    assert status_of(fn, d, P, P, 32, P, P, None, None, 5) == INVALID       # unknown activation
+    assert status_of(fn, d, P, P, 32, P, P, None, None, 0, None, None, -2) == INVALID
+    assert status_of(fn, d, P, P, 32, None, P) == INVALID                   # no pointwise weights
+    assert status_of(fn, d, P, P, 32, P + 1, P) == MISALIGNED
+    assert status_of(fn, d, P, P, 32, P, P, P + 1) == MISALIGNED            # dw_scale
+    slice_over = B.make_desc(2, 64, 8, 8, 3, 1, 1, dtype="bf16", out_c_offset=10, out_c_total=40)
+    assert status_of(fn, slice_over, P, P, 32, P, P) == INVALID
+    assert B.dwconv2d_separable_plan_name(slice_over, 30) == "septc"        # 10 + 30 <= 40
+    assert B.dwconv2d_separable_plan_name(slice_over, 31) == "invalid"
+    assert status_of(fn, B.make_desc(0, 64, 8, 8, 3, 1, 1, dtype="bf16"), None, P, 32, P, None) == 0
+    # tensor-core kernel: 16-bit, 3x3 / 5x5, stride 1 / 2, dilation 1, m = 1, C % 64 == 0
+    sp = B.dwconv2d_separable_plan_name
+    assert sp(B.make_desc(64, 128, 56, 56, 3, 1, 1, dtype="bf16"), 128) == "septc"
+    assert sp(B.make_desc(64, 512, 14, 14, 3, 2, 1, dtype="f16"), 1024) == "septc"
+    assert sp(B.make_desc(8, 64, 30, 30, 5, 2, 2, dtype="bf16"), 96) == "septc"
+    assert sp(B.make_desc(8, 64, 30, 30, 3, 1, 1), 96) == "generic"                     # fp32
+    assert sp(B.make_desc(8, 96, 30, 30, 3, 1, 1, dtype="bf16"), 96) == "generic"       # C % 64
+    assert sp(B.make_desc(8, 64, 30, 30, 7, 1, 3, dtype="bf16"), 96) == "generic"       # 7x7
+    assert sp(B.make_desc(8, 64, 30, 30, 3, 1, 2, 2, dtype="bf16"), 96) == "generic"    # dilation
+    assert sp(B.make_desc(8, 64, 30, 30, 3, 1, 1, multiplier=2, dtype="bf16"), 96) == "generic"
+    # the generic kernel stages one pixel's C*m fp32 values in at most 96 KB
+    assert sp(B.make_desc(1, 24577, 4, 4, 3, 1, 1), 8) == "invalid"
+
+
 def test_workspace_checks(lib):
     d = B.make_desc(4, 8, 16, 16, 3, 1, 1)
     need = B.dwconv2d_bwd_weight_workspace_size(d)

@@ -223,3 +223,89 @@ def test_nhwc_full_size_mobilenet_layer_sampled():
     cv = oconv(L, N=len(nsel), C=len(csel))
     ref = oracle.fwd(cv, inp.x.f64[np.ix_(nsel, csel)], inp.w.f64[csel])
     assert_close(got[np.ix_(nsel, csel)], ref, "f32", 9, "mobilenet nhwc")
+
+
+# ------------------------------------------------- depthwise-separable block
+# (layer, cout, out_c_offset, out_c_total, dw act, pw act, expected kernel)
+SEP_CASES = [
+    (WL.Layer(N=2, C=64, H=14, W=14, k=3, s=1, p=1, dtype="bf16"), 64, 0, 0, "relu6", "relu6", "septc"),
+    (WL.Layer(N=3, C=128, H=17, W=19, k=3, s=2, p=1, dtype="f16"), 40, 0, 0, "relu", "none", "septc"),
+    (WL.Layer(N=2, C=64, H=7, W=7, k=3, s=1, p=1, dtype="bf16"), 256, 0, 0, "relu6", "relu", "septc"),
+    (WL.Layer(N=2, C=128, H=9, W=9, k=5, s=1, p=2, dtype="f16"), 300, 0, 0, "none", "relu6", "septc"),
+    (WL.Layer(N=1, C=64, H=30, W=30, k=5, s=2, p=2, dtype="bf16"), 96, 0, 0, "relu6", "none", "septc"),
+    (WL.Layer(N=5, C=64, H=4, W=4, k=3, s=1, p=1, dtype="bf16"), 32, 0, 0, "relu", "relu", "septc"),
+    (WL.Layer(N=2, C=64, H=56, W=56, k=3, s=1, p=1, dtype="bf16"), 128, 8, 136, "relu6", "relu6", "septc"),
+    (WL.Layer(N=2, C=64, H=23, W=23, k=3, s=1, p=1, dtype="f16"), 48, 3, 55, "relu6", "none", "septc"),
+    (WL.Layer(N=2, C=24, H=15, W=15, k=3, s=1, p=1), 20, 0, 0, "relu6", "relu", "generic"),
+    (WL.Layer(N=2, C=48, H=12, W=12, k=3, s=2, p=1, dtype="bf16"), 64, 0, 0, "relu", "relu6", "generic"),
+    (WL.Layer(N=2, C=16, H=10, W=10, k=3, s=1, p=1, m=2, dtype="f16"), 24, 0, 0, "none", "none", "generic"),
+    (WL.Layer(N=2, C=64, H=13, W=13, k=3, s=1, p=2, d=2, dtype="bf16"), 32, 0, 0, "relu", "relu", "generic"),
+]
+SEP_IDS = ["k3s1_bf16_14", "k3s2_f16_cout40", "k3_bf16_7x7_pack2", "k5s1_f16_cout300", "k5s2_bf16",
+           "bf16_4x4_pack8", "slice_aligned", "slice_unaligned", "f32_generic", "C48_generic",
+           "m2_generic", "d2_generic"]
+
+
+def sep_run(L, cout, off, ctot, a1, a2, seed=0):
+    th = torch()
+    inp, x = nhwc_inputs(L, seed)
+    s1, h1 = WL.make_scale_shift(L, seed)
+    wp, s2, h2 = WL.make_pointwise(L, cout, seed)
+    d = B.make_desc(**L.desc_kwargs(), out_c_offset=off, out_c_total=ctot)
+    y = empty_dev((L.N, L.Ho, L.Wo, ctot or cout), L.dtype, fill=-5.0)
+    B.dwconv2d_separable_nhwc(d, x, to_dev(inp.w), cout, to_dev(wp), y, dw_scale=to_dev(s1), dw_shift=to_dev(h1),
+                              dw_act=a1, pw_scale=to_dev(s2), pw_shift=to_dev(h2), pw_act=a2)
+    th.cuda.synchronize()
+    got = np.ascontiguousarray(to_f64(y).transpose(0, 3, 1, 2))
+    return d, got, (inp, s1, h1, wp, s2, h2)
+
+
+@pytest.mark.parametrize("L,cout,off,ctot,a1,a2,family", SEP_CASES, ids=SEP_IDS)
+def test_separable_block_vs_oracle(L, cout, off, ctot, a1, a2, family):
+    d, got, (inp, s1, h1, wp, s2, h2) = sep_run(L, cout, off, ctot, a1, a2)
+    assert B.dwconv2d_separable_plan_name(d, cout) == family
+    ref = oracle.separable(oconv(L), inp.x.f64, inp.w.f64, s1.f64, h1.f64, a1, wp.f64, s2.f64, h2.f64, a2)
+    assert_close(got[:, off:off + cout], ref, L.dtype, L.k * L.k + L.OC, f"separable {L.label()}")
+    if ctot:
+        assert np.all(got[:, :off] == -5.0) and np.all(got[:, off + cout:] == -5.0)
+
+
+def test_separable_block_full_size_mobilenet_sampled():
+    """A full-size MobileNet block (64 x 128 x 56 x 56 bf16, 3x3, 1x1 to 128
+    channels), compared with the oracle on three whole samples."""
+    L = WL.Layer(N=64, C=128, H=56, W=56, k=3, s=1, p=1, dtype="bf16")
+    d, got, (inp, s1, h1, wp, s2, h2) = sep_run(L, 128, 0, 0, "relu6", "relu6")
+    assert B.dwconv2d_separable_plan_name(d, 128) == "septc"
+    nsel = [0, 33, 63]
+    ref = oracle.separable(oconv(L, N=3), inp.x.f64[nsel], inp.w.f64, s1.f64, h1.f64, "relu6", wp.f64, s2.f64,
+                           h2.f64, "relu6")
+    assert_close(got[nsel], ref, "bf16", 9 + 128, "mobilenet separable block")
+
+
+def test_separable_block_deterministic_and_misaligned_weights_fall_back():
+    """Two runs agree bit for bit; a pointwise weight pointer that is not
+    16-byte aligned cannot be a tensor-map base and runs the generic kernel,
+    within tolerance of the same oracle."""
+    th = torch()
+    L = WL.Layer(N=2, C=64, H=20, W=20, k=3, s=1, p=1, dtype="bf16")
+    _, a, args = sep_run(L, 64, 0, 0, "relu6", "relu")
+    _, b, _ = sep_run(L, 64, 0, 0, "relu6", "relu")
+    assert np.array_equal(a, b)
+    inp, s1, h1, wp, s2, h2 = args
+    _, x = nhwc_inputs(L)
+    wpd = to_dev(wp)
+    buf = th.empty(wpd.numel() + 1, dtype=wpd.dtype, device="cuda")
+    wmis = buf[1:].view(wpd.shape)
+    wmis.copy_(wpd)
+    d = B.make_desc(**L.desc_kwargs())
+    y = empty_dev((L.N, L.Ho, L.Wo, 64), "bf16")
+    B.dwconv2d_separable_nhwc(d, x, to_dev(inp.w), 64, wmis, y, dw_scale=to_dev(s1), dw_shift=to_dev(h1),
+                              dw_act="relu6", pw_scale=to_dev(s2), pw_shift=to_dev(h2), pw_act="relu")
+    th.cuda.synchronize()
+    got = np.ascontiguousarray(to_f64(y).transpose(0, 3, 1, 2))
+    ref = oracle.separable(oconv(L), inp.x.f64, inp.w.f64, s1.f64, h1.f64, "relu6", wp.f64, s2.f64, h2.f64, "relu")
+    assert_close(got, ref, "bf16", 9 + 64, "misaligned pointwise weights")
+
+
+def test_no_bounded_wait_gave_up_in_fused_kernels():
+    assert B.dwconv_device_timeouts() == 0
