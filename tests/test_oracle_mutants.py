@@ -23,8 +23,8 @@ MUTANTS = {
     "fwd_channel_map": ("const int64_t n = t / OC, oc = t % OC, c = oc / d->m;",
                         "const int64_t n = t / OC, oc = t % OC, c = oc % d->C;"),
     "fwd_bias_dropped": ("if (bias) acc += bias[oc];", ""),
-    "fwd_slice_offset_dropped": ("double* yp = y + (n * d->c_total + d->off + oc) * Ho * Wo;",
-                                 "double* yp = y + (n * d->c_total + oc) * Ho * Wo;"),
+    "fwd_slice_offset_dropped": ("kw;\n    double* yp = y + (n * d->c_total + d->off + oc) * Ho * Wo;",
+                                 "kw;\n    double* yp = y + (n * d->c_total + oc) * Ho * Wo;"),
     "bwd_data_no_divisibility": ("if (num_h < 0 || num_h % d->sh != 0) continue;",
                                  "if (num_h < 0) continue;"),
     "bwd_data_dilation_sign": ("const int64_t num_w = iw + d->pw - b * d->dw;",
