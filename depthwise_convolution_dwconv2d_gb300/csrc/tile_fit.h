@@ -65,5 +65,24 @@ inline int64_t wgrad_min_bytes(int K, int S, int D, int M, int64_t Wo, int es) {
   return (tr * pitch + M * R * gpitch) * es;
 }
 
+// Weight gradient: the most bands of output rows its planner can split a
+// plane into (its band search, 32 KB per slice, with the widest pitch; a
+// narrower pitch gives taller bands, never more of them).
+inline int64_t wgrad_max_bands(int K, int S, int D, int M, int64_t Ho, int64_t Wo, int es) {
+  const int64_t R = S == 1 ? 2 : 1, V = 4;
+  const int64_t cb = (Wo + V - 1) / V;
+  const int64_t need = (cb - 1) * V * S + fit_max_shift(es) + (V - 1) * S + (int64_t)(K - 1) * D + 1 + 3;
+  const int64_t pitch = fit_rup(need, fit_pitch_align(es));
+  const int64_t gpitch = fit_rup(cb * V, fit_pitch_align(es));
+  auto bytes_of = [&](int64_t th) { return (((th - 1) * S + (int64_t)(K - 1) * D + 1) * pitch + M * th * gpitch) * es; };
+  const int64_t target = 32 * 1024;
+  int64_t th = (Ho + R - 1) / R * R;
+  if (bytes_of(th) > target) {
+    th = R;
+    while (bytes_of(th + R) <= target) th += R;
+  }
+  return (Ho + th - 1) / th;
+}
+
 }  // namespace tile
 }  // namespace dwconv

@@ -61,9 +61,24 @@ int64_t wgrad_nb(const Conv& c) {
   return nb;
 }
 
+// Chunks of the (sample, band) slices of each channel. From the sample
+// count above; when the batch is too small for about sixteen units per SM
+// (e.g. 2 samples of 64 channels), whole samples are split further, up to
+// one chunk per band the planner can cut a plane into (the kernel spreads
+// its actual bands over the chunks; a chunk past the last slice writes a
+// zero partial). Depends on the descriptor alone.
 int wgrad_chunks(const Conv& c) {
+  if (c.N <= 0) return 1;
   const int64_t nb = wgrad_nb(c);
-  return c.N > 0 ? (int)((c.N + nb - 1) / nb) : 1;
+  const int64_t by_samples = (c.N + nb - 1) / nb;
+  const int64_t wanted = (152 * 16 + c.C - 1) / c.C;
+  if (by_samples >= wanted || nb > 1) return (int)by_samples;
+  const int es = c.dtype == DWCONV_F32 ? 4 : 2;
+  int64_t chunks = c.N * wgrad_max_bands(c.kh, c.sh, c.dh, c.m, c.Ho, c.Wo, es);
+  if (chunks > wanted) chunks = wanted;
+  if (chunks < by_samples) chunks = by_samples;
+  if (chunks > 65535) chunks = 65535;
+  return (int)chunks;
 }
 
 cudaError_t wgrad(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s) {

@@ -25,7 +25,7 @@ namespace tile {
 namespace {
 
 struct WCfg {
-  int nb;          // batch samples per chunk
+  int spc;         // slices (sample, band) per chunk: chunk q holds slices [q spc, (q + 1) spc)
   int chunks;
   int th, nbands;  // output rows per band, bands per plane
   int tr, pitch;   // x tile rows / pitch (elements)
@@ -68,7 +68,8 @@ wgrad_kernel(Conv c, WCfg g, const __grid_constant__ CUtensorMap xmap,
   T* const buf[2] = {reinterpret_cast<T*>(smraw), reinterpret_cast<T*>(smraw) + g.stage_elems};
   float* red = reinterpret_cast<float*>(reinterpret_cast<T*>(smraw) + 2 * g.stage_elems);  // [warps][NV]
   const int64_t units = c.C * g.chunks;
-  // slices of a unit: (sample n0 + sl / nbands, band sl % nbands)
+  // slices of a unit: global slice q * spc + sl = (sample, band) =
+  // (slice / nbands, slice % nbands) for sl < unit_slices(u)
   // unit u = chunk * C + channel (units < 2^32: the host caps chunks)
   auto unit_split = [&](int64_t uu, int64_t& ch, int& chunk) {
     uint32_t q;
@@ -79,15 +80,16 @@ wgrad_kernel(Conv c, WCfg g, const __grid_constant__ CUtensorMap xmap,
     int64_t ch_;
     int chunk;
     unit_split(u, ch_, chunk);
-    const int64_t n0 = (int64_t)chunk * g.nb;
-    const int64_t nn = (c.N - n0) < g.nb ? (c.N - n0) : g.nb;
-    return nn > 0 ? (int)(nn * g.nbands) : 0;
+    const int64_t s_first = (int64_t)chunk * g.spc;
+    const int64_t left = c.N * g.nbands - s_first;
+    return left > 0 ? (int)(left < g.spc ? left : g.spc) : 0;
   };
   auto issue = [&](int64_t u, int s0, T* dst, uint64_t* bar) {
     int64_t ch;
     int chunk;
     unit_split(u, ch, chunk);
-    const int64_t n0 = (int64_t)chunk * g.nb;
+    // (one band per plane: slices are samples and n0 the chunk's first one)
+    const int64_t n0 = (int64_t)chunk * g.spc;
     const int nsl = unit_slices(u);
     const int ns = (nsl - s0) < g.ppc ? (nsl - s0) : g.ppc;
     T* xs = dst;
@@ -120,10 +122,10 @@ wgrad_kernel(Conv c, WCfg g, const __grid_constant__ CUtensorMap xmap,
         } else {
           tma::mbar_expect_tx(bar, g.tma_slice_bytes * ns);
           for (int q = 0; q < ns; ++q) {
-            const int sl = s0 + q;
+            const int64_t sl = (int64_t)chunk * g.spc + s0 + q;  // global slice
             uint32_t sq;
             const int oh0 = (int)g.d_nbands.divmod((uint32_t)sl, sq) * g.th;
-            const int n = (int)(n0 + sq);
+            const int n = (int)sq;
             tma::load_4d(xs + q * g.xstride, &xmap, g.xix0, oh0 * S - c.ph, (int)ch, n, bar);
             tma::load_4d(gs + q * g.gstride, &gmap, 0, oh0, (int)(c.off + ch * M), n, bar);
           }
@@ -137,10 +139,10 @@ wgrad_kernel(Conv c, WCfg g, const __grid_constant__ CUtensorMap xmap,
                     (int)c.Ho, (int)c.Wo, 0, g.th, g.thdiv, 0, g.gmode);
     } else {
       for (int q = 0; q < ns; ++q) {
-        const int sl = s0 + q;
+        const int64_t sl = (int64_t)chunk * g.spc + s0 + q;  // global slice
         uint32_t sq;
         const int oh0 = (int)g.d_nbands.divmod((uint32_t)sl, sq) * g.th;
-        const int64_t n = n0 + sq;
+        const int64_t n = sq;
         issue_tile<T>(xs + q * g.xstride, 1, g.xstride, g.pitch, [&](int) { return x + c.x_base(n, ch); },
                       (int)c.H, (int)c.W, oh0 * S - c.ph, g.tr, g.trdiv, g.xix0, g.xmode);
         issue_tile<T>(gs + q * g.gstride, M, g.g_elems, g.gpitch,
@@ -187,7 +189,7 @@ wgrad_kernel(Conv c, WCfg g, const __grid_constant__ CUtensorMap xmap,
     int64_t chu;
     int chunku;
     unit_split(u, chu, chunku);
-    const int64_t n0u = (int64_t)chunku * g.nb;
+    const int64_t n0u = (int64_t)chunku * g.spc;  // (used by whole-plane staging only)
     const int per = (int)g.d_per.d;
     for (int it = threadIdx.x; it < ns * per; it += kNT) {
       uint32_t q_, rbi_;
@@ -311,9 +313,8 @@ cudaError_t run_wgrad_t(const Conv& c, const void* x, const void* gy, float* ws,
   constexpr int ES = sizeof(T);
   constexpr int PA = 16 / ES > 4 ? 16 / ES : 4;  // pitch alignment (elements)
   WCfg g{};
+  if (chunks < 1) return cudaErrorInvalidConfiguration;
   g.chunks = chunks;
-  g.nb = (int)wgrad_nb(c);
-  if (c.N > 0 && (c.N + g.nb - 1) / g.nb != chunks) return cudaErrorInvalidConfiguration;
   g.cb = (int)((c.Wo + V - 1) / V);
   g.gpitch = round_up((int64_t)g.cb * V, PA);
   int ix0 = 0, shift = 0, gshift = 0;
@@ -337,6 +338,15 @@ cudaError_t run_wgrad_t(const Conv& c, const void* x, const void* gy, float* ws,
   g.rb = (int)(th / R);
   g.nbands = (int)((c.Ho + th - 1) / th);
   g.d_nbands = FastDiv((uint32_t)g.nbands);
+  // the chunks split the N x nbands slices evenly (chunks past the last
+  // slice stay empty and write zero partials)
+  {
+    const int64_t total = c.N * g.nbands;
+    int64_t spc = (total + chunks - 1) / chunks;
+    if (spc < 1) spc = 1;
+    if (total > (int64_t)0x7fffffff) return cudaErrorInvalidConfiguration;
+    g.spc = (int)spc;
+  }
   g.tr = (int)tr_of(th);
   g.x_elems = g.tr * g.pitch;
   g.g_elems = (int)(th * g.gpitch);
@@ -348,7 +358,7 @@ cudaError_t run_wgrad_t(const Conv& c, const void* x, const void* gy, float* ws,
   int64_t ppc = (2 * kNT + items - 1) / items;
   const int64_t cap = target / bytes_of(th);
   if (ppc > cap) ppc = cap;
-  const int64_t slices = (int64_t)g.nb * g.nbands;
+  const int64_t slices = g.spc;
   if (ppc > slices) ppc = slices;
   if (ppc < 1) ppc = 1;
   // tensor copies when both tensors allow 16-byte rows and the boxes fit
