@@ -32,6 +32,7 @@ struct MultiArgs {
   int tr[3], tile_elems[3];   // bwd: per-branch tiles
   int iy0[3], ix0[3], mode[3];  // tile origins relative to the band, copy modes
   FastDiv trdiv[3];
+  FastDiv d_prb[3], d_cbq[3];   // fwd: division by items per row block, by cb * Q
 };
 
 struct MCfg {
@@ -56,34 +57,37 @@ __device__ __forceinline__ void conv_dl(int dl, const TS* t, int pitch, int tr0,
   }
 }
 
+// One R x V output block of branch b (filter wr, bias bv already in
+// registers): item -> (row block, row phase, column block, column phase).
 template <int K, int D, typename T>
-__device__ __forceinline__ void fwd_branch(const Conv& c, const MultiArgs& a, int b, const T* t,
-                                           int pitch, int item, int64_t n, int64_t ch, int oh0,
-                                           int band_rows, const T* w, const T* bias, T* y) {
+__device__ __forceinline__ void fwd_branch(const Conv& c, const MultiArgs& a, int b, const T* t, int pitch,
+                                           int item, int64_t n, int64_t ch, int oh0, int band_rows,
+                                           const float (&wr)[K * K], float bv, T* y) {
   constexpr int Q = D;
-  const int per_rb = a.cb[b] * Q * Q;
-  const int rbi = item / per_rb;
-  int rem = item - rbi * per_rb;
-  const int qy = rem / (a.cb[b] * Q);
-  rem -= qy * a.cb[b] * Q;
-  const int cbi = rem / Q;
-  const int qx = rem - cbi * Q;
-  float wr[K * K];
-#pragma unroll
-  for (int i = 0; i < K * K; ++i) wr[i] = ld(w + ch * (K * K) + i);
-  const float bv = bias ? ld(bias + ch) : 0.f;
+  uint32_t rbi_, qy_;
+  uint32_t rem = a.d_prb[b].divmod((uint32_t)item, rbi_);
+  rem = a.d_cbq[b].divmod(rem, qy_);
+  const int cbi = (int)rem / Q;
+  const int qx = (int)rem - cbi * Q;
   float acc[kR][kV];
 #pragma unroll
   for (int r = 0; r < kR; ++r)
 #pragma unroll
     for (int v = 0; v < kV; ++v) acc[r][v] = bv;
-  const int ohr = rbi * Q * kR + qy;
+  const int ohr = (int)rbi_ * Q * kR + (int)qy_;
   const int owb = cbi * Q * kV + qx;
   conv_dl<K, D, Q>(a.dl[b], t, pitch, ohr + a.oy[b], owb + a.ox[b], wr, acc);
   const bool vec = Q == 1 && c.Wo % 4 == 0 &&
                    (reinterpret_cast<uintptr_t>(y) % (4 * sizeof(T))) == 0;
   store_block<T, kR, kV, Q>(y + (n * c.ctot + a.off[b] + ch) * c.Ho * c.Wo, c.Wo, oh0 + ohr, owb,
                             band_rows - ohr, (int)c.Wo, acc, vec, false);
+}
+
+template <int K, typename T>
+__device__ __forceinline__ void load_filter(const T* w, const T* bias, int64_t ch, float (&wr)[K * K], float& bv) {
+#pragma unroll
+  for (int i = 0; i < K * K; ++i) wr[i] = ld(w + ch * (K * K) + i);
+  bv = bias ? ld(bias + ch) : 0.f;
 }
 
 template <typename T, int K, int NB, int D0, int D1, int D2>
@@ -119,21 +123,29 @@ fwd_multi_kernel(Conv c, MCfg g, MultiArgs a, const T* __restrict__ x, T* __rest
     const int np = (int)((nplanes - p0) < g.ppc ? (nplanes - p0) : g.ppc);
     const int oh0 = band * g.th;
     const int band_rows = (int)((c.Ho - oh0) < g.th ? (c.Ho - oh0) : g.th);
+    // A thread's items run through the planes and, within a plane, through
+    // the branches in order: each branch's filter is loaded once per plane.
+    int curp = -1, have = 0;
+    int64_t n = 0, ch = 0;
+    float w0[K * K], w1[K * K], w2[K * K], b0 = 0.f, b1 = 0.f, b2 = 0.f;
     for (int it = threadIdx.x; it < np * per_plane; it += kNT) {
       const int pl = it / per_plane;
       const int q = it - pl * per_plane;
-      int64_t n, ch;
-      c.split(p0 + pl, n, ch);
+      if (pl != curp) {
+        curp = pl;
+        have = 0;
+        c.split(p0 + pl, n, ch);
+      }
       const T* t = cur + pl * g.tile_elems;
       if (q < i0) {
-        fwd_branch<K, D0>(c, a, 0, t, g.pitch, q, n, ch, oh0, band_rows, (const T*)a.w[0],
-                          (const T*)a.bias[0], y);
+        if (!(have & 1)) load_filter<K>((const T*)a.w[0], (const T*)a.bias[0], ch, w0, b0), have |= 1;
+        fwd_branch<K, D0>(c, a, 0, t, g.pitch, q, n, ch, oh0, band_rows, w0, b0, y);
       } else if (q < i0 + i1) {
-        fwd_branch<K, D1>(c, a, 1, t, g.pitch, q - i0, n, ch, oh0, band_rows, (const T*)a.w[1],
-                          (const T*)a.bias[1], y);
+        if (!(have & 2)) load_filter<K>((const T*)a.w[1], (const T*)a.bias[1], ch, w1, b1), have |= 2;
+        fwd_branch<K, D1>(c, a, 1, t, g.pitch, q - i0, n, ch, oh0, band_rows, w1, b1, y);
       } else if (NB > 2) {
-        fwd_branch<K, (NB > 2 ? D2 : 1)>(c, a, 2, t, g.pitch, q - i0 - i1, n, ch, oh0, band_rows,
-                                         (const T*)a.w[2], (const T*)a.bias[2], y);
+        if (!(have & 4)) load_filter<K>((const T*)a.w[2], (const T*)a.bias[2], ch, w2, b2), have |= 4;
+        fwd_branch<K, (NB > 2 ? D2 : 1)>(c, a, 2, t, g.pitch, q - i0 - i1, n, ch, oh0, band_rows, w2, b2, y);
       }
     }
     __syncthreads();
@@ -287,6 +299,8 @@ cudaError_t run_fwd_multi(const Conv* cs, const void* x, const void* const* w, c
   for (int b = 0; b < NB; ++b) {
     a.rb[b] = (int)(th / (Ds[b] * kR));
     a.items[b] = a.rb[b] * a.cb[b] * Ds[b] * Ds[b];
+    a.d_prb[b] = FastDiv((uint32_t)(a.cb[b] * Ds[b] * Ds[b]));
+    a.d_cbq[b] = FastDiv((uint32_t)(a.cb[b] * Ds[b]));
     items += a.items[b];
   }
   a.iy0[0] = -hh;
