@@ -13,10 +13,13 @@ The six workloads (``depthwise_convolution_dwconv2d_gb300.workloads``):
   multiplier -- 128 x 256 x 28^2, 5x5, multiplier 2, bias, bf16;
   infer      -- the MobileNet table again as an inference forward in
                 channels-last layout with a fused scale / shift / ReLU6
-                epilogue, fp32 and bf16 (forward only: one call per layer).
+                epilogue, fp32 and bf16 (forward only: one call per layer);
+  separable  -- the MobileNet table as depthwise-separable blocks (3x3
+                depthwise + 1x1, both with scale / shift / ReLU6), bf16,
+                channels-last, one call per block.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                    [--workload all|pr1|mobilenet|largek|multidil|multiplier|infer]
+                    [--workload all|pr1|mobilenet|largek|multidil|multiplier|infer|separable]
 
 With no flags every workload is timed, one after another, and ONE JSON line
 is printed (rank 0). Its headline (``value``, ``config``, ``roofline``,
@@ -50,7 +53,7 @@ sys.path.insert(0, ROOT)
 METRIC = "dwconv fwd/bwd-data/bwd-weight ms, achieved GB/s or TFLOP/s vs roofline"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-ORDER = ("pr1", "mobilenet", "largek", "multidil", "multiplier", "infer")
+ORDER = ("pr1", "mobilenet", "largek", "multidil", "multiplier", "infer", "separable")
 HEADLINE = "largek"
 WORKLOAD_TEXT = {
     "pr1": "PR1 layer, fp32 NCHW, N=1 C=32 H=W=28, 3x3, stride 1, pad 1, fwd+bwd_data+bwd_weight",
@@ -65,6 +68,9 @@ WORKLOAD_TEXT = {
                   "fwd+bwd_data+bwd_weight+bias grad",
     "infer": "MobileNet-shape inference forward, channels-last (NHWC in and out), N=64, 3x3 pad 1, fused "
              "per-channel scale + shift + ReLU6 (a folded batch norm), fp32 and bf16; same layer table as mobilenet",
+    "separable": "MobileNet-shape depthwise-separable blocks, channels-last, bf16, N=64: 3x3 depthwise + scale + "
+                 "shift + ReLU6, then 1x1 to the next layer's channels + scale + shift + ReLU6, in one call per "
+                 "block; same layer table as mobilenet",
 }
 # Source files whose device code each kernel family runs: a committed DRAM
 # traffic figure is reported only while these files are unchanged.
@@ -78,6 +84,7 @@ FAMILY_SOURCES = {
     "tcwgrad": ("common.cuh", "plan.h", "tma.cuh", "tma.cu", "wgrad_tc.cu", "generic.cu"),
     "generic": ("common.cuh", "plan.h", "generic.cu"),
     "nhwc": ("common.cuh", "plan.h", "nhwc.h", "nhwc.cu", "tile.cuh", "tma.cuh", "tma.cu"),
+    "septc": ("common.cuh", "plan.h", "nhwc.h", "separable.cu", "tc.cuh", "tile.cuh", "tma.cuh", "tma.cu", "vec.cuh"),
 }
 
 
@@ -96,6 +103,8 @@ def build_workload(name):
         return [WL.multidil()]
     if name == "infer":
         return WL.mobilenet_infer()
+    if name == "separable":
+        return WL.mobilenet_separable()
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -126,6 +135,13 @@ def layer_calls(item):
         return out
     L = item
     es = 4 if L.dtype == "f32" else 2
+    if isinstance(L, WL.SepLayer):
+        # depthwise FMAs (valid taps) + 1x1 MACs; bytes: x, y, both filters, both scale / shift pairs
+        fma = L.N * L.OC * valid_taps(L.Ho, L.k, L.s, L.p, L.d, L.H) * valid_taps(L.Wo, L.k, L.s, L.p, L.d, L.W)
+        fma += L.N * L.Ho * L.Wo * L.OC * L.cout
+        nb = (L.N * L.C * L.H * L.W + L.N * L.cout * L.Ho * L.Wo + L.OC * (L.k * L.k + 2)
+              + L.cout * (L.OC + 2)) * es
+        return [("fwd", nb, fma, 1)]
     if isinstance(L, WL.InferLayer):
         fma = L.N * L.OC * valid_taps(L.Ho, L.k, L.s, L.p, L.d, L.H) * valid_taps(L.Wo, L.k, L.s, L.p, L.d, L.W)
         nb = L.N * L.C * L.H * L.W * es + L.N * L.OC * L.Ho * L.Wo * es + L.OC * (L.k * L.k + 2) * es
@@ -312,7 +328,13 @@ def oracle_sample(items, budget_s):
             cv = oracle.Conv(N=n, C=L.C, H=L.H, W=L.W, kh=L.k, kw=L.k, sh=L.s, sw=L.s, ph=L.p, pw=L.p,
                              dh=L.d, dw=L.d, m=L.m)
             b = inp.b.f64 if inp.b is not None else None
-            if isinstance(L, WL.InferLayer):
+            if isinstance(L, WL.SepLayer):
+                sc, sh = WL.make_scale_shift(L)
+                wp, psc, psh = WL.make_pointwise(L, L.cout)
+                t0 = time.perf_counter()
+                oracle.separable(cv, inp.x.f64, inp.w.f64, sc.f64, sh.f64, L.act, wp.f64, psc.f64, psh.f64, L.act)
+                t_total += time.perf_counter() - t0
+            elif isinstance(L, WL.InferLayer):
                 # the oracle is layout-free: NCHW arrays, the same function
                 sc, sh = WL.make_scale_shift(L)
                 t0 = time.perf_counter()
@@ -344,7 +366,9 @@ def oracle_sample(items, budget_s):
             c = full_c
             n = max(1, min(full_n, int(scale)))
         t, by, fm = run(n, c)
-    passes = "fwd with epilogue" if all(isinstance(i, WL.InferLayer) for i in items) else "fwd+bwd_data+bwd_weight"
+    passes = ("separable block (depthwise + 1x1, both epilogues)" if all(isinstance(i, WL.SepLayer) for i in items)
+              else "fwd with epilogue" if all(isinstance(i, WL.InferLayer) for i in items)
+              else "fwd+bwd_data+bwd_weight")
     desc = (f"first {n} sample(s)" + ("" if c >= full_c else f" and first {c} channels") +
             f" of every layer, {passes}, one timed pass")
     return by / t, fm / t, t, desc
@@ -450,6 +474,26 @@ def setup_workload(name, items, dev, stream, hc, out_host):
         L = item
         xd = "uniform" if L.x_dist == "uniform" else "normal"
         wstd = L.w_std if L.w_std is not None else 1.0 / L.k
+        if isinstance(L, WL.SepLayer):
+            xh = hc.get(("x_nhwc", (L.N, L.H, L.W, L.C), L.dtype, xd), lambda L=L: _NHWC(WL.make_x(L)))
+            wh = hc.get(("w", (L.OC, L.k, L.k), L.dtype, 0, wstd), lambda L=L: WL.make_w(L))
+            sch = hc.get(("scale", (L.OC,), L.dtype), lambda L=L: WL.make_scale_shift(L)[0])
+            shh = hc.get(("shift", (L.OC,), L.dtype), lambda L=L: WL.make_scale_shift(L)[1])
+            pws = [hc.get(("pw", i, (L.cout, L.OC), L.dtype), lambda L=L, i=i: WL.make_pointwise(L, L.cout)[i])
+                   for i in range(3)]
+            d = B.make_desc(**L.desc_kwargs())
+            x, w, sc, sh = xh.to(dev), wh.to(dev), sch.to(dev), shh.to(dev)
+            wp, psc, psh = (t.to(dev) for t in pws)
+            y = torch.empty((L.N, L.Ho, L.Wo, L.cout), dtype=tdt(L.dtype), device=dev)
+            cl = layer_calls(L)
+            idx0 = len(calls)
+            calls.append(("fwd", L.label(), fam(B.dwconv2d_separable_plan_name(d, L.cout), L.dtype), cl[0][1],
+                          cl[0][2], 1,
+                          lambda d=d, x=x, w=w, y=y, sc=sc, sh=sh, wp=wp, psc=psc, psh=psh, L=L:
+                          B.dwconv2d_separable_nhwc(d, x, w, L.cout, wp, y, sc, sh, L.act, psc, psh, L.act, stream)))
+            h2d = [(xh, x), (wh, w), (sch, sc), (shh, sh)] + list(zip(pws, (wp, psc, psh)))
+            groups.append((h2d, list(range(idx0, len(calls))), [(y, host_out(y))]))
+            continue
         if isinstance(L, WL.InferLayer):
             xh = hc.get(("x_nhwc", (L.N, L.H, L.W, L.C), L.dtype, xd), lambda L=L: _NHWC(WL.make_x(L)))
             wh = hc.get(("w", (L.OC, L.k, L.k), L.dtype, 0, wstd), lambda L=L: WL.make_w(L))
@@ -647,7 +691,7 @@ def time_workload(name, items, args, dev, stream, world, dist, peaks, fma_tflops
     for key, f in fams.items():
         pass_, plan, dt = key.split(":")
         family = plan.replace("multi-", "")
-        if family in ("ibgemm", "tcwgrad"):
+        if family in ("ibgemm", "tcwgrad", "septc"):
             bp = ("tensor", tc_peak, tc_src)
         elif fma_tflops:
             bp = ("alu", fma_tflops, fma_src)

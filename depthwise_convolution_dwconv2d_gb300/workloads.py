@@ -112,6 +112,25 @@ def mobilenet_infer(N=64, dtypes=("f32", "bf16")):
             for dt in dtypes for c, h, s in layers]
 
 
+@dataclass
+class SepLayer(InferLayer):
+    """A depthwise-separable block (inference, channels-last): the depthwise
+    layer with its scale / shift / activation, then a 1x1 layer to `cout`
+    channels with its own scale / shift / activation."""
+    cout: int = 0
+
+
+def mobilenet_separable(N=64, dtype="bf16"):
+    """The MobileNet layer table as depthwise-separable blocks: each 1x1 layer
+    outputs the input channels of the table's next row (the last keeps 1024),
+    MobileNet v1's channel sequence."""
+    layers = [(64, 112, 2), (128, 56, 1), (128, 56, 2), (256, 28, 1), (256, 28, 2),
+              (512, 14, 1), (512, 14, 2), (1024, 7, 2)]
+    outs = [c for c, _, _ in layers[1:]] + [1024]
+    return [SepLayer(N=N, C=c, H=h, W=h, k=3, s=s, p=1, dtype=dtype, cout=co, name=f"sep_C{c}_H{h}_s{s}_o{co}")
+            for (c, h, s), co in zip(layers, outs)]
+
+
 def pr1():
     return [Layer(N=1, C=32, H=28, W=28, k=3, s=1, p=1, name="pr1_C32_H28")]
 
