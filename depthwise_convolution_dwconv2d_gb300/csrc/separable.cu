@@ -61,6 +61,9 @@ constexpr int kM = 128;          // pixel slots per tile (MMA M)
 constexpr int kKc = 64;          // channels per K chunk (one 128-byte swizzle row)
 constexpr int kMaxStages = 2;
 constexpr unsigned kSleepNs = 64;
+// Epilogue-2 table: scale2 and shift2 of every output channel (fp32), staged
+// once per CTA when cout is at most kEpiTab channels.
+constexpr int64_t kEpiTab = 2048;
 
 struct SCfg {
   int nimg, th, tw, twp;   // tile: images x rows x (valid columns, column slots)
@@ -125,6 +128,10 @@ septc_kernel(SCfg g, const __grid_constant__ CUtensorMap xmap, const __grid_cons
   __shared__ int abort_s;
   unsigned char* sm = smdyn + ((1024 - (tma::smem_u32(smdyn) & 1023)) & 1023);
   float* const tab0 = reinterpret_cast<float*>(sm + (size_t)g.stages * g.stage_bytes);
+  // epilogue-2 scale / shift table after the two filter-table slots (empty
+  // when cout is too large: the epilogue then reads global memory)
+  float* const etab = tab0 + 2 * g.tab_floats;
+  const bool use_etab = g.cout <= kEpiTab;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     for (int s = 0; s < g.stages; ++s) {
@@ -216,6 +223,13 @@ septc_kernel(SCfg g, const __grid_constant__ CUtensorMap xmap, const __grid_cons
     const int r_ = rem / g.twp, col = rem - r_ * g.twp;
     const T* s2 = reinterpret_cast<const T*>(ep.s2);
     const T* h2 = reinterpret_cast<const T*>(ep.h2);
+    if (use_etab) {
+      for (int64_t i = p; i < g.cout; i += 128) {
+        etab[2 * i] = s2 ? ld(s2 + i) : 1.f;
+        etab[2 * i + 1] = h2 ? ld(h2 + i) : 0.f;
+      }
+      asm volatile("bar.sync 2, 128;\n" ::: "memory");  // the four epilogue warps
+    }
     uint32_t tiles = 0;
     for (int64_t u = u0; u < u1; ++u, ++tiles) {
       const UnitPos up = unit_pos(g, u);
@@ -237,7 +251,15 @@ septc_kernel(SCfg g, const __grid_constant__ CUtensorMap xmap, const __grid_cons
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int c = co + i < g.cout ? co + i : co;
-            const float sc = s2 ? ld(s2 + c) : 1.f, sh = h2 ? ld(h2 + c) : 0.f;
+            float sc, sh;
+            if (use_etab) {
+              const float2 t2 = *reinterpret_cast<const float2*>(etab + 2 * c);
+              sc = t2.x;
+              sh = t2.y;
+            } else {
+              sc = s2 ? ld(s2 + c) : 1.f;
+              sh = h2 ? ld(h2 + c) : 0.f;
+            }
             v[i] = epi_act(fmaf(v[i], sc, sh), ep.a2);
           }
           if (g.vec_out && co + 16 <= g.cout) {
@@ -267,29 +289,56 @@ septc_kernel(SCfg g, const __grid_constant__ CUtensorMap xmap, const __grid_cons
     const bool used = p0 < g.nimg * per_img;
     const T* s1 = reinterpret_cast<const T*>(ep.s1);
     const T* h1 = reinterpret_cast<const T*>(ep.h1);
-    const int tabn = K * K * kKc + 2 * kKc;
+    // A chunk's filters as [tap][channel], then scale1 and shift1, in one of
+    // two table slots (chunk t in slot t & 1). Every builder holds its share
+    // of the next chunk's table in registers, loaded one chunk ahead so the
+    // global loads overlap the current chunk's work, and stores it just
+    // before the builders' barrier: the slot it writes was last read two
+    // chunks earlier, which every builder finished before the previous
+    // barrier.
+    constexpr int tabn = K * K * kKc + 2 * kKc;
+    constexpr int TPT = (tabn + kBuilders - 1) / kBuilders;  // table values per builder
+    float pre[TPT];
+    auto fetch_tab = [&](int kc) {
+      const int c0 = kc * kKc;
+#pragma unroll
+      for (int q = 0; q < TPT; ++q) {
+        const int i = tid + q * kBuilders;
+        float v = 0.f;
+        if (i < K * K * kKc) {
+          const int cl = i / (K * K), tap = i - cl * (K * K);
+          v = ld(wd + (int64_t)(c0 + cl) * (K * K) + tap);
+        } else if (i < K * K * kKc + kKc) {
+          v = s1 ? ld(s1 + c0 + (i - K * K * kKc)) : 1.f;
+        } else if (i < tabn) {
+          v = h1 ? ld(h1 + c0 + (i - K * K * kKc - kKc)) : 0.f;
+        }
+        pre[q] = v;
+      }
+    };
+    auto store_tab = [&](float* tab) {
+#pragma unroll
+      for (int q = 0; q < TPT; ++q) {
+        const int i = tid + q * kBuilders;
+        if (i < K * K * kKc) {
+          const int cl = i / (K * K), tap = i - cl * (K * K);
+          tab[tap * kKc + cl] = pre[q];
+        } else if (i < tabn) {
+          tab[i] = pre[q];
+        }
+      }
+    };
+    if (u0 < u1) fetch_tab(0);
+    uint32_t t = 0;
     Ring r;
     for (int64_t u = u0; u < u1; ++u) {
-      for (int kc = 0; kc < g.nkc; ++kc, r.next(g.stages)) {
-        // this chunk's filters as [tap][channel], then scale1 and shift1
-        float* tab = tab0 + r.s * g.tab_floats;
-        const int c0 = kc * kKc;
-        for (int i = tid; i < tabn; i += kBuilders) {
-          float v;
-          if (i < K * K * kKc) {
-            const int cl = i / (K * K), tap = i - cl * (K * K);
-            tab[tap * kKc + cl] = ld(wd + (int64_t)(c0 + cl) * (K * K) + tap);
-            continue;
-          } else if (i < K * K * kKc + kKc) {
-            const int cl = i - K * K * kKc;
-            v = s1 ? ld(s1 + c0 + cl) : 1.f;
-          } else {
-            const int cl = i - K * K * kKc - kKc;
-            v = h1 ? ld(h1 + c0 + cl) : 0.f;
-          }
-          tab[i] = v;
-        }
+      for (int kc = 0; kc < g.nkc; ++kc, r.next(g.stages), ++t) {
+        float* tab = tab0 + (t & 1) * g.tab_floats;
+        store_tab(tab);
         builders_sync();
+        // the next chunk of this CTA's walk: kc + 1, or chunk 0 of the next unit
+        if (kc + 1 < g.nkc) fetch_tab(kc + 1);
+        else if (u + 1 < u1) fetch_tab(0);
         if (!*abortp && !tc::wait(&fullB[r.s], r.ph, timeouts, abortp, kSleepNs)) *abortp = 1;
         unsigned char* A = A_of(r.s);
         uint4 out[4];
@@ -403,7 +452,10 @@ sep_generic_kernel(Conv c, int64_t cout, int64_t ctot, int64_t off, int P, const
 
 // ---- host planning ----------------------------------------------------------------
 
-size_t tc_smem(const SCfg& g) { return 1024 + (size_t)g.stages * g.stage_bytes + (size_t)g.stages * g.tab_floats * 4; }
+inline size_t epi_tab_bytes(const SCfg& g) { return g.cout <= kEpiTab ? (size_t)g.cout * 8 : 0; }
+size_t tc_smem(const SCfg& g) {
+  return 1024 + (size_t)g.stages * g.stage_bytes + (size_t)2 * g.tab_floats * 4 + epi_tab_bytes(g);
+}
 
 // Tile shape and stages for the tensor-core kernel; false if the shape is
 // not one it takes or nothing fits in shared memory.
