@@ -79,11 +79,12 @@ FAMILY_SOURCES = {
              "tile_fwd.cu", "tile_fwd_impl.cuh", "tile_bwd2.cu", "tile_bwd2_impl.cuh", "tile_wgrad.cu",
              "tile_wgrad_impl.cuh", "tile_multi.cu", "generic.cu"),
     "plane": ("common.cuh", "plan.h", "plane.cu", "generic.cu"),
-    "large": ("common.cuh", "plan.h", "tile.cuh", "large.cu", "large_impl.cuh", "generic.cu"),
+    "large": ("common.cuh", "plan.h", "tile.cuh", "large.cu", "large_entries.h", "large_common.cuh",
+              "large_pair.cuh", "large_impl.cuh", "generic.cu"),
     "ibgemm": ("common.cuh", "plan.h", "tma.cuh", "tma.cu", "ibgemm.cu"),
     "tcwgrad": ("common.cuh", "plan.h", "tma.cuh", "tma.cu", "wgrad_tc.cu", "generic.cu"),
     "generic": ("common.cuh", "plan.h", "generic.cu"),
-    "nhwc": ("common.cuh", "plan.h", "nhwc.h", "nhwc.cu", "tile.cuh", "tma.cuh", "tma.cu"),
+    "nhwc": ("common.cuh", "plan.h", "nhwc.h", "nhwc.cu", "tile.cuh", "tma.cuh", "tma.cu", "vec.cuh"),
     "septc": ("common.cuh", "plan.h", "nhwc.h", "separable.cu", "tc.cuh", "tile.cuh", "tma.cuh", "tma.cu", "vec.cuh"),
 }
 
@@ -259,7 +260,8 @@ def family_digest(family):
 
 def ncu_traffic(key, family):
     """Per-launch DRAM bytes of one kernel family from the committed ncu
-    figures, if they were taken on the family's current sources; else None."""
+    figures (one representative layer, scaled to the workload's batch), if
+    they were taken on the family's current sources; else None."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
@@ -269,7 +271,7 @@ def ncu_traffic(key, family):
         return None
     if not e or e.get("digest") != family_digest(family):
         return None
-    return e.get("bytes_per_launch")
+    return e
 
 
 def fma_probe_tflops(dev, stream):
@@ -536,9 +538,12 @@ def setup_workload(name, items, dev, stream, hc, out_host):
     return calls, groups
 
 
-def roofline_of(fam_rec, bound_peaks, hbm_peak, hbm_kind, traffic):
+def roofline_of(fam_rec, bound_peaks, hbm_peak, hbm_kind, traffic_entry):
     """Roofline of one kernel family: t_roof = max(bytes / HBM peak, FLOPs /
-    compute peak), frac = t_roof / t_measured; achieved in the bound's unit."""
+    compute peak), frac = t_roof / t_measured; achieved in the bound's unit.
+    traffic: DRAM bytes of one launch of the family's representative layer
+    (ncu), beside that launch's algorithmic bytes."""
+    traffic = traffic_entry.get("bytes_per_launch") if traffic_entry else None
     ms, by, fma = fam_rec["ms"], fam_rec["bytes"], fam_rec["fma"]
     comp_kind, comp_peak, comp_src = bound_peaks
     t_mem = by / (hbm_peak * 1e6)           # ms
@@ -697,7 +702,11 @@ def time_workload(name, items, args, dev, stream, world, dist, peaks, fma_tflops
             bp = ("alu", fma_tflops, fma_src)
         else:
             bp = ("alu", 80.5, "nominal FP32 FMA rate (152 x 128 x 2 x 2.07 GHz)")
-        r = roofline_of(f, bp, hbm_peak, hbm_kind, ncu_traffic(f"{name}:{key}", family))
+        te = ncu_traffic(f"{name}:{key}", family)
+        r = roofline_of(f, bp, hbm_peak, hbm_kind, te)
+        if te:
+            r["traffic_layer"] = te.get("layer")
+            r["traffic_layer_algorithmic_bytes"] = te.get("algorithmic_bytes_per_launch")
         r.update({"kernel": key, "calls": f["calls"], "launches": f["launches"], "ms": round(f["ms"], 4),
                   "share": round(f["ms"] / ms_per_step, 4)})
         rl[key] = r

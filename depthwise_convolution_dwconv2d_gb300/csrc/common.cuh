@@ -87,6 +87,23 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
   return __float2bfloat16_rn(v);
 }
 
+// Two fp32 values in one 64-bit register (lane 0 in the low word), the operand
+// form of the two-lane FP32 instructions of the sm_100 family.
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pack_f32x2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack_f32x2(f32x2 v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+// d = a * b + d on both lanes (PTX fma.rn.f32x2): each lane is one IEEE fused
+// multiply-add with a single rounding, the same as fmaf on that lane.
+__device__ __forceinline__ void fma_f32x2(f32x2& d, f32x2 a, f32x2 b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+
 // plain (coherent) load for data this kernel may also write
 template <typename T> __device__ __forceinline__ float ld_rw(const T* p) { return to_f<T>(*p); }
 

@@ -46,15 +46,11 @@
 namespace dwconv {
 namespace large {
 
-typedef unsigned long long u64;
+typedef f32x2 u64;
 
 // d = w * x + d on both 32-bit lanes of the 64-bit operands.
-__device__ __forceinline__ void fma2(u64& d, u64 w, u64 x) {
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(w), "l"(x));
-}
-__device__ __forceinline__ void unpack2(u64 v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
+__device__ __forceinline__ void fma2(u64& d, u64 w, u64 x) { fma_f32x2(d, w, x); }
+__device__ __forceinline__ void unpack2(u64 v, float& lo, float& hi) { unpack_f32x2(v, lo, hi); }
 
 // Physical pair index of logical pair column q in a staged row: a 16-byte
 // gap (two pairs) after every V pairs.

@@ -343,38 +343,44 @@ septc_kernel(SCfg g, const __grid_constant__ CUtensorMap xmap, const __grid_cons
         unsigned char* A = A_of(r.s);
         uint4 out[4];
         if (used && !*abortp) {
-          float acc[4][8];
+          // channels (2i, 2i + 1) of the thread's 8 are one lane pair of the
+          // two-lane FMA (taps, inputs and sums pair up without moves)
+          f32x2 accp[4][4];
 #pragma unroll
           for (int p = 0; p < 4; ++p)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[p][e] = 0.f;
+            for (int i = 0; i < 4; ++i) accp[p][i] = 0ull;
           const unsigned char* box = box_of(r.s);
 #pragma unroll
           for (int a = 0; a < K; ++a) {
-            float wr[K][8];
+            f32x2 wr[K][4];
 #pragma unroll
             for (int b = 0; b < K; ++b) {
-              const float4 f0 = *reinterpret_cast<const float4*>(tab + (a * K + b) * kKc + 8 * j);
-              const float4 f1 = *reinterpret_cast<const float4*>(tab + (a * K + b) * kKc + 8 * j + 4);
-              wr[b][0] = f0.x; wr[b][1] = f0.y; wr[b][2] = f0.z; wr[b][3] = f0.w;
-              wr[b][4] = f1.x; wr[b][5] = f1.y; wr[b][6] = f1.z; wr[b][7] = f1.w;
+              const ulonglong2 f0 = *reinterpret_cast<const ulonglong2*>(tab + (a * K + b) * kKc + 8 * j);
+              const ulonglong2 f1 = *reinterpret_cast<const ulonglong2*>(tab + (a * K + b) * kKc + 8 * j + 4);
+              wr[b][0] = f0.x; wr[b][1] = f0.y; wr[b][2] = f1.x; wr[b][3] = f1.y;
             }
             const unsigned char* rowp =
                 box + ((size_t)((img * g.bh + r_ * S + a) * g.bw + col0 * S)) * 128 + j * 16;
 #pragma unroll
             for (int jj = 0; jj < WIN; ++jj) {
-              float xv[8];
-              unpack16<T>(*reinterpret_cast<const uint4*>(rowp + jj * 128), xv);
+              f32x2 xv[4];
+              unpack16_pairs<T>(*reinterpret_cast<const uint4*>(rowp + jj * 128), xv);
 #pragma unroll
               for (int p = 0; p < 4; ++p) {
                 const int b = jj - p * S;
                 if (b >= 0 && b < K) {
 #pragma unroll
-                  for (int e = 0; e < 8; ++e) acc[p][e] = fmaf(wr[b][e], xv[e], acc[p][e]);
+                  for (int i = 0; i < 4; ++i) fma_f32x2(accp[p][i], wr[b][i], xv[i]);
                 }
               }
             }
           }
+          float acc[4][8];
+#pragma unroll
+          for (int p = 0; p < 4; ++p)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) unpack_f32x2(accp[p][i], acc[p][2 * i], acc[p][2 * i + 1]);
           const float* st = tab + K * K * kKc + 8 * j;
 #pragma unroll
           for (int p = 0; p < 4; ++p) {

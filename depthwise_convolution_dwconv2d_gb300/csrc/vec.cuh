@@ -40,6 +40,31 @@ __device__ __forceinline__ void unpack16<__half>(const uint4& u, float* o) {
   }
 }
 
+// 16 bytes of storage-type values -> fp32 lane pairs (channels 2i, 2i + 1 in
+// pair i), exact
+template <typename T>
+__device__ __forceinline__ void unpack16_pairs(const uint4& u, f32x2* o);
+template <>
+__device__ __forceinline__ void unpack16_pairs<float>(const uint4& u, f32x2* o) {
+  o[0] = ((f32x2)u.y << 32) | u.x;
+  o[1] = ((f32x2)u.w << 32) | u.z;
+}
+template <>
+__device__ __forceinline__ void unpack16_pairs<__nv_bfloat16>(const uint4& u, f32x2* o) {
+  const uint32_t v[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) o[i] = ((f32x2)(v[i] & 0xffff0000u) << 32) | (uint32_t)(v[i] << 16);
+}
+template <>
+__device__ __forceinline__ void unpack16_pairs<__half>(const uint4& u, f32x2* o) {
+  const uint32_t v[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&v[i]));
+    o[i] = pack_f32x2(f.x, f.y);
+  }
+}
+
 // fp32 -> 16 bytes of storage-type values (round to nearest even)
 template <typename T>
 __device__ __forceinline__ uint4 pack16(const float* a);
