@@ -25,7 +25,9 @@ SYMBOLS = ("dwconv2d_output_shape", "dwconv2d_fwd", "dwconv2d_bwd_data",
            "dwconv2d_bwd_data_multi", "dwconv_status_string", "dwconv2d_plan_name",
            "dwconv2d_multi_plan_name", "dwconv_fma_probe", "dwconv2d_bwd_weight_noalloc",
            "dwconv_device_timeouts", "dwconv_wait_selftest", "dwconv2d_fwd_epilogue",
-           "dwconv2d_fwd_nhwc", "dwconv2d_separable_nhwc", "dwconv2d_separable_plan_name")
+           "dwconv2d_fwd_nhwc", "dwconv2d_separable_nhwc", "dwconv2d_separable_plan_name",
+           "dwconv2d_filter_cache_size", "dwconv2d_filter_cache_build", "dwconv2d_fwd_cached",
+           "dwconv2d_bwd_data_cached")
 
 # dwconv_act_t
 ACTS = {"none": 0, "relu": 1, "relu6": 2}
@@ -108,9 +110,14 @@ def load():
     lib.dwconv_device_timeouts.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     lib.dwconv_fma_probe.argtypes = [ctypes.c_int, ctypes.c_int, vp, vp]
     lib.dwconv_wait_selftest.argtypes = [ctypes.c_uint, vp]
+    lib.dwconv2d_filter_cache_size.argtypes = [P, ctypes.c_int]
+    lib.dwconv2d_filter_cache_size.restype = ctypes.c_size_t
+    lib.dwconv2d_filter_cache_build.argtypes = [P, ctypes.c_int, vp, vp, ctypes.c_size_t, vp]
+    lib.dwconv2d_fwd_cached.argtypes = [P, vp, vp, ctypes.c_size_t, vp, vp, vp]
+    lib.dwconv2d_bwd_data_cached.argtypes = [P, vp, vp, ctypes.c_size_t, vp, ctypes.c_int, vp]
     for name in SYMBOLS:
         if name not in ("dwconv2d_bwd_weight_workspace_size", "dwconv_status_string", "dwconv2d_plan_name",
-                        "dwconv2d_multi_plan_name", "dwconv2d_separable_plan_name"):
+                        "dwconv2d_multi_plan_name", "dwconv2d_separable_plan_name", "dwconv2d_filter_cache_size"):
             getattr(lib, name).restype = st
     _lib = lib
     return lib
@@ -209,6 +216,37 @@ def dwconv2d_bwd_weight_noalloc(desc: Desc, x, gy, gw, gbias, stream=None):
     _check(load().dwconv2d_bwd_weight_noalloc(ctypes.byref(desc), _ptr(x), _ptr(gy), _ptr(gw),
                                               _ptr(gbias), _stream(stream)),
            "dwconv2d_bwd_weight_noalloc")
+
+
+def dwconv2d_filter_cache_size(desc: Desc, pass_: int) -> int:
+    """Bytes of the filter cache of pass 0 (forward) or 1 (grad-input); 0 if none."""
+    return int(load().dwconv2d_filter_cache_size(ctypes.byref(desc), int(pass_)))
+
+
+def _nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+def dwconv2d_filter_cache_build(desc: Desc, pass_: int, w, cache, cache_bytes=None, stream=None):
+    if cache_bytes is None:
+        cache_bytes = _nbytes(cache)
+    _check(load().dwconv2d_filter_cache_build(ctypes.byref(desc), int(pass_), _ptr(w), _ptr(cache),
+                                              int(cache_bytes), _stream(stream)),
+           "dwconv2d_filter_cache_build")
+
+
+def dwconv2d_fwd_cached(desc: Desc, x, cache, bias, y, cache_bytes=None, stream=None):
+    if cache_bytes is None:
+        cache_bytes = _nbytes(cache)
+    _check(load().dwconv2d_fwd_cached(ctypes.byref(desc), _ptr(x), _ptr(cache), int(cache_bytes), _ptr(bias),
+                                      _ptr(y), _stream(stream)), "dwconv2d_fwd_cached")
+
+
+def dwconv2d_bwd_data_cached(desc: Desc, gy, cache, gx, accumulate=0, cache_bytes=None, stream=None):
+    if cache_bytes is None:
+        cache_bytes = _nbytes(cache)
+    _check(load().dwconv2d_bwd_data_cached(ctypes.byref(desc), _ptr(gy), _ptr(cache), int(cache_bytes), _ptr(gx),
+                                           int(accumulate), _stream(stream)), "dwconv2d_bwd_data_cached")
 
 
 def _desc_array(descs):

@@ -283,6 +283,63 @@ dwconv_status_t dwconv2d_bwd_weight(const dwconv2d_desc_t* desc, const void* x, 
   return cuda_status(run_bwd_weight(p, c, x, gy, gw, gbias, (float*)workspace, stream));
 }
 
+size_t dwconv2d_filter_cache_size(const dwconv2d_desc_t* desc, int pass) {
+  Conv c;
+  if (make_conv(desc, &c) != DWCONV_OK || (pass != 0 && pass != 1)) return 0;
+  return ibc::cache_bytes(c, pass == 1);
+}
+
+namespace {
+
+// Checks shared by the cache build and the cached calls: a cached form for
+// this pass, a cache pointer that is 16-byte aligned and large enough.
+dwconv_status_t check_cache(const Conv& c, bool flip, const void* cache, size_t cache_bytes) {
+  const size_t need = ibc::cache_bytes(c, flip);
+  if (need == 0) return DWCONV_ERR_UNSUPPORTED;
+  if (!cache || cache_bytes < need) return DWCONV_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(cache) % 16 != 0) return DWCONV_ERR_MISALIGNED;
+  return DWCONV_OK;
+}
+
+}  // namespace
+
+dwconv_status_t dwconv2d_filter_cache_build(const dwconv2d_desc_t* desc, int pass, const void* w, void* cache,
+                                            size_t cache_bytes, cudaStream_t stream) {
+  Conv c;
+  DW_TRY(make_conv(desc, &c));
+  if (pass != 0 && pass != 1) return DWCONV_ERR_INVALID_ARG;
+  DW_TRY(check_cache(c, pass == 1, cache, cache_bytes));
+  DW_TRY(check_ptr(w, esize(c.dtype), true));
+  return cuda_status(ibc::build(c, pass == 1, w, cache, stream));
+}
+
+dwconv_status_t dwconv2d_fwd_cached(const dwconv2d_desc_t* desc, const void* x, const void* cache,
+                                    size_t cache_bytes, const void* bias, void* y, cudaStream_t stream) {
+  Conv c;
+  DW_TRY(make_conv(desc, &c));
+  DW_TRY(check_cache(c, false, cache, cache_bytes));
+  const int es = esize(c.dtype);
+  DW_TRY(check_ptr(bias, es, false));
+  if (c.N == 0) return DWCONV_OK;
+  if (!ibc::call_supported(c, false)) return DWCONV_ERR_UNSUPPORTED;
+  DW_TRY(check_ptr(x, 16, true));
+  DW_TRY(check_ptr(y, es, true));
+  return cuda_status(ibc::run(c, false, x, cache, bias, y, false, stream));
+}
+
+dwconv_status_t dwconv2d_bwd_data_cached(const dwconv2d_desc_t* desc, const void* gy, const void* cache,
+                                         size_t cache_bytes, void* gx, int accumulate, cudaStream_t stream) {
+  Conv c;
+  DW_TRY(make_conv(desc, &c));
+  DW_TRY(check_cache(c, true, cache, cache_bytes));
+  if (accumulate != 0 && accumulate != 1) return DWCONV_ERR_INVALID_ARG;
+  if (c.N == 0) return DWCONV_OK;
+  if (!ibc::call_supported(c, true)) return DWCONV_ERR_UNSUPPORTED;
+  DW_TRY(check_ptr(gy, 16, true));
+  DW_TRY(check_ptr(gx, esize(c.dtype), true));
+  return cuda_status(ibc::run(c, true, gy, cache, nullptr, gx, accumulate != 0, stream));
+}
+
 dwconv_status_t dwconv2d_fwd_multi(int nbranch, const dwconv2d_desc_t* descs, const void* x,
                                    const void* const* w, const void* const* bias, void* y,
                                    cudaStream_t stream) {

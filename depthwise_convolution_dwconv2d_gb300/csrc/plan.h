@@ -97,6 +97,16 @@ cudaError_t fwd(const Conv& c, const void* x, const void* w, const void* b, void
 cudaError_t bwd_data(const Conv& c, const void* gy, const void* w, void* gx, bool acc, cudaStream_t s);
 }  // namespace ibg
 
+namespace ibc {
+// ibgemm_cache.cu: the implicit batched GEMM with its expanded filter (the
+// kernel-side im2col) built once into a caller-owned cache
+size_t cache_bytes(const Conv& c, bool flip);   // 0: the shape has no cached form
+bool call_supported(const Conv& c, bool flip);  // this call's batch / plane sizes run on the cached kernel
+cudaError_t build(const Conv& c, bool flip, const void* w, void* cache, cudaStream_t s);
+cudaError_t run(const Conv& c, bool flip, const void* in, const void* cache, const void* bias, void* out, bool acc,
+                cudaStream_t s);
+}  // namespace ibc
+
 namespace wtc {
 // wgrad_tc.cu: large-kernel weight gradient (first pass) on the tensor cores,
 // 16-bit data, stride 1; cudaErrorNotSupported when this call's x or grad_out

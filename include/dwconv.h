@@ -228,6 +228,59 @@ dwconv_status_t dwconv2d_separable_nhwc(const dwconv2d_desc_t* desc, const void*
                                         const void* w_pw, const void* pw_scale, const void* pw_shift,
                                         int pw_act, void* y, cudaStream_t stream);
 
+/* Filter cache for repeated large-kernel calls with a fixed filter
+ * (inference; or the forward and grad-input of one training step). Source:
+ * the MegEngine large-kernel depthwise article, section on the
+ * implicit-batched-GEMM algorithm: each channel's convolution is a GEMM
+ * whose A operand is the im2col of the filter,
+ *   T_c[oh*W + ow, ih*W + iw] = w_c[ih - oh + ph][iw - ow + pw]  (0 off the filter)
+ * and, when shapes stay fixed between calls, that filter-side im2col can be
+ * prepared ahead of the calls instead of inside each one.
+ *
+ * A cached form exists for fp16 / bf16 descriptors with stride 1, dilation
+ * 1, one filter per channel, pad_h <= kh - 1, pad_w <= kw - 1 and, for the
+ * pass's correlation, equal input and output row widths W that divide 64
+ * (8, 16, 32 or 64; for both passes: Wo == W, i.e. 2 * pad_w == kw - 1),
+ * when one channel's expanded filter fits in shared memory beside the
+ * kernel's input stages: C x NS x W x 128 bytes in all, NS = the number of
+ * filter-row offsets a 128-position tile meets (38 for 31x31 at W = 32; at
+ * W = 64 filters up to 21 rows have a cached form, 27 and 31 do not).
+ * Pass 0 caches the forward's filter, pass 1 the grad-input's (the filter
+ * rotated by 180 degrees); each pass needs its own cache.
+ *
+ * dwconv2d_filter_cache_size: bytes of the cache (0 when the descriptor is
+ * invalid, pass is not 0 or 1, or the shape has no cached form). It depends
+ * on C, W, the kernel size, the padding and the dtype -- not on N or H, so
+ * one cache serves every batch and height of that layer.
+ *
+ * dwconv2d_filter_cache_build: expands w ([C, kh, kw], desc->dtype) into
+ * `cache` (caller-owned device memory, 16-byte aligned, cache_bytes >= the
+ * size above); one launch on `stream`, nothing else written. Build again
+ * whenever w changes.
+ *
+ * dwconv2d_fwd_cached / dwconv2d_bwd_data_cached: the results of
+ * dwconv2d_fwd / dwconv2d_bwd_data (same arguments, slices, accumulate
+ * flag and rounding), with the filter taken from a cache that
+ * dwconv2d_filter_cache_build made for the same pass from a descriptor that
+ * agrees in C, W, kh, kw, pad_h, pad_w and dtype (the library cannot check
+ * the cache's contents; another cache gives wrong results, not an error).
+ * x (resp. gy) must be 16-byte aligned.
+ *
+ * Errors: DWCONV_ERR_UNSUPPORTED when the shape has no cached form;
+ * DWCONV_ERR_WORKSPACE when cache is NULL or cache_bytes is too small;
+ * DWCONV_ERR_MISALIGNED for a cache or x / gy not 16-byte aligned (other
+ * pointers: their element size); DWCONV_ERR_INVALID_ARG for pass not 0 or 1
+ * and as dwconv2d_fwd / dwconv2d_bwd_data otherwise. An empty batch
+ * (N == 0) enqueues nothing. */
+size_t dwconv2d_filter_cache_size(const dwconv2d_desc_t* desc, int pass);
+dwconv_status_t dwconv2d_filter_cache_build(const dwconv2d_desc_t* desc, int pass, const void* w,
+                                            void* cache, size_t cache_bytes, cudaStream_t stream);
+dwconv_status_t dwconv2d_fwd_cached(const dwconv2d_desc_t* desc, const void* x, const void* cache,
+                                    size_t cache_bytes, const void* bias, void* y, cudaStream_t stream);
+dwconv_status_t dwconv2d_bwd_data_cached(const dwconv2d_desc_t* desc, const void* gy, const void* cache,
+                                         size_t cache_bytes, void* gx, int accumulate,
+                                         cudaStream_t stream);
+
 /* Fused multi-branch forward (the DynamicConvolutionOperator's single launch
  * for dilation 1, 3, 5 whose results are stored straight into slices of one
  * concatenated tensor): nbranch (1..8) descriptors over the same x. All

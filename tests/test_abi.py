@@ -303,3 +303,57 @@ def test_every_odd_large_filter_has_a_specialised_plan(lib):
             p16 = [B.dwconv2d_plan_name(d16, p) for p in range(3)]
             assert p16[:2] == (["tile"] * 2 if k == 7 else ["ibgemm"] * 2), (k, h, p16)
             assert p16[2] == ("tile" if k == 7 else "tcwgrad"), (k, h, p16)
+
+
+def test_filter_cache_sizes_and_argument_checks(lib):
+    """Cache sizes of the large-kernel layers (C x strips x W rows of 128
+    bytes; 38 strips for 31x31 at width 32, 44 at width 16, 23 for 21x21 at
+    width 64), shapes without a cached form (31x31 at width 64: its 35
+    strips of 8 KB do not fit in shared memory), and the checks before any
+    launch."""
+    size = B.dwconv2d_filter_cache_size
+    for W, k, strips in ((32, 31, 38), (16, 31, 44), (64, 21, 23), (32, 13, 22)):
+        for pass_ in (0, 1):
+            assert size(B.make_desc(64, 384, W, W, k, 1, k // 2, dtype="f16"), pass_) == 384 * strips * W * 128
+    d = B.make_desc(64, 384, 32, 32, 31, 1, 15, dtype="bf16")
+    # independent of N and H
+    assert size(B.make_desc(1, 384, 7, 32, 31, 1, 15, dtype="bf16"), 0) == size(d, 0)
+    assert size(B.make_desc(0, 384, 32, 32, 31, 1, 15, dtype="bf16"), 0) == size(d, 0)
+    assert size(B.make_desc(300, 384, 32, 32, 31, 1, 15, dtype="bf16"), 0) == size(d, 0)
+    for bad in (B.make_desc(64, 384, 32, 32, 31, 1, 15),                      # fp32
+                B.make_desc(64, 384, 48, 48, 31, 1, 15, dtype="f16"),         # 48 does not divide 64
+                B.make_desc(64, 384, 24, 24, 11, 1, 2, dtype="f16"),          # Wo != W
+                B.make_desc(64, 384, 32, 32, 31, 2, 15, dtype="f16"),         # stride 2
+                B.make_desc(64, 384, 32, 32, 31, 1, 15, 2, dtype="f16"),      # dilation 2
+                B.make_desc(8, 16, 32, 32, 31, 1, 15, multiplier=2, dtype="f16"),
+                B.make_desc(8, 16, 4, 4, 3, 1, 1, dtype="f16"),               # width 4
+                B.make_desc(64, 384, 64, 64, 31, 1, 15, dtype="f16"),         # strips do not fit
+                B.make_desc(64, 384, 64, 64, 27, 1, 13, dtype="bf16")):
+        assert size(bad, 0) == 0 and size(bad, 1) == 0
+    assert size(d, 2) == 0 and size(d, -1) == 0
+    need = size(d, 0)
+    build, fc, bc = B.dwconv2d_filter_cache_build, B.dwconv2d_fwd_cached, B.dwconv2d_bwd_data_cached
+    assert status_of(build, d, 2, P, P, need, 0) == INVALID
+    assert status_of(build, d, 0, P, None, need, 0) == WORKSPACE
+    assert status_of(build, d, 0, P, P, need - 1, 0) == WORKSPACE
+    assert status_of(build, d, 0, P, P + 8, need, 0) == MISALIGNED
+    assert status_of(build, d, 0, P + 1, P, need, 0) == MISALIGNED
+    assert status_of(build, d, 0, None, P, need, 0) == INVALID
+    f32 = B.make_desc(64, 384, 32, 32, 31, 1, 15)
+    assert status_of(build, f32, 0, P, P, 1 << 30, 0) == UNSUPPORTED
+    assert status_of(fc, f32, P, P, None, P, 1 << 30, 0) == UNSUPPORTED
+    assert status_of(fc, d, P, None, None, P, need, 0) == WORKSPACE
+    assert status_of(fc, d, P, P, None, P, need - 2, 0) == WORKSPACE
+    assert status_of(fc, d, P + 8, P, None, P, need, 0) == MISALIGNED     # x on the 16-byte grid
+    assert status_of(fc, d, P, P, P + 1, P, need, 0) == MISALIGNED        # bias
+    assert status_of(fc, d, P, P, None, None, need, 0) == INVALID
+    big = B.make_desc(64, 384, 64, 64, 31, 1, 15, dtype="bf16")
+    assert status_of(fc, big, P, P, None, P, 1 << 30, 0) == UNSUPPORTED
+    assert status_of(build, big, 0, P, P, 1 << 30, 0) == UNSUPPORTED
+    assert status_of(bc, d, P, P, P, 2, need, 0) == INVALID                 # accumulate not 0 / 1
+    assert status_of(bc, d, P, P, P + 1, 0, need, 0) == MISALIGNED
+    assert status_of(bc, d, P + 8, P, P, 0, need, 0) == MISALIGNED
+    # empty batch: a valid no-op once the cache checks out
+    e = B.make_desc(0, 384, 32, 32, 31, 1, 15, dtype="bf16")
+    assert status_of(fc, e, None, P, None, None, need, 0) == 0
+    assert status_of(bc, e, None, P, None, 0, need, 0) == 0
