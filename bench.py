@@ -2,7 +2,7 @@
 """Benchmark: one step = forward, backward-data and backward-weight of every
 layer of a synthetic depthwise workload, through libdwconv's C ABI.
 
-The six workloads (``depthwise_convolution_dwconv2d_gb300.workloads``):
+The eight workloads (``depthwise_convolution_dwconv2d_gb300.workloads``):
   pr1        -- N=1 C=32 28x28 3x3 fp32 ("Spatial Depthwise Convolution on
                 the GPU #3057", its smallest MobileNet layer);
   mobilenet  -- the PR's MobileNet layer table at batch 64, fp32;
@@ -16,10 +16,14 @@ The six workloads (``depthwise_convolution_dwconv2d_gb300.workloads``):
                 epilogue, fp32 and bf16 (forward only: one call per layer);
   separable  -- the MobileNet table as depthwise-separable blocks (3x3
                 depthwise + 1x1, both with scale / shift / ReLU6), bf16,
-                channels-last, one call per block.
+                channels-last, one call per block;
+  largek_infer -- the fp16 large-kernel layers (k 13..31) as an inference
+                forward with a static filter: the filter cache (the
+                kernel-side im2col of the MegEngine article) is built once
+                before timing where the shape has a cached form.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                    [--workload all|pr1|mobilenet|largek|multidil|multiplier|infer|separable]
+                    [--workload all|pr1|mobilenet|largek|multidil|multiplier|infer|separable|largek_infer]
 
 With no flags every workload is timed, one after another, and ONE JSON line
 is printed (rank 0). Its headline (``value``, ``config``, ``roofline``,
@@ -53,7 +57,7 @@ sys.path.insert(0, ROOT)
 METRIC = "dwconv fwd/bwd-data/bwd-weight ms, achieved GB/s or TFLOP/s vs roofline"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-ORDER = ("pr1", "mobilenet", "largek", "multidil", "multiplier", "infer", "separable")
+ORDER = ("pr1", "mobilenet", "largek", "multidil", "multiplier", "infer", "separable", "largek_infer")
 HEADLINE = "largek"
 WORKLOAD_TEXT = {
     "pr1": "PR1 layer, fp32 NCHW, N=1 C=32 H=W=28, 3x3, stride 1, pad 1, fwd+bwd_data+bwd_weight",
@@ -71,6 +75,10 @@ WORKLOAD_TEXT = {
     "separable": "MobileNet-shape depthwise-separable blocks, channels-last, bf16, N=64: 3x3 depthwise + scale + "
                  "shift + ReLU6, then 1x1 to the next layer's channels + scale + shift + ReLU6, in one call per "
                  "block; same layer table as mobilenet",
+    "largek_infer": "Large-kernel inference forward with a static filter, fp16 NCHW, N=64 C=384, H=W in {32,48,64}, "
+                    "k in {13,21,27,31}, stride 1, pad k//2: the filter cache (kernel-side im2col) built once before "
+                    "timing where the shape has a cached form (H=W=32; H=W=64 with k<=21), the uncached forward "
+                    "elsewhere",
 }
 # Source files whose device code each kernel family runs: a committed DRAM
 # traffic figure is reported only while these files are unchanged.
@@ -86,6 +94,7 @@ FAMILY_SOURCES = {
     "generic": ("common.cuh", "plan.h", "generic.cu"),
     "nhwc": ("common.cuh", "plan.h", "nhwc.h", "nhwc.cu", "tile.cuh", "tma.cuh", "tma.cu", "vec.cuh"),
     "septc": ("common.cuh", "plan.h", "nhwc.h", "separable.cu", "tc.cuh", "tile.cuh", "tma.cuh", "tma.cu", "vec.cuh"),
+    "ibgemm-cached": ("common.cuh", "plan.h", "tc.cuh", "tile.cuh", "tma.cuh", "tma.cu", "ibgemm_cache.cu"),
 }
 
 
@@ -106,6 +115,8 @@ def build_workload(name):
         return WL.mobilenet_infer()
     if name == "separable":
         return WL.mobilenet_separable()
+    if name == "largek_infer":
+        return WL.largek_infer()
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -146,6 +157,14 @@ def layer_calls(item):
     if isinstance(L, WL.InferLayer):
         fma = L.N * L.OC * valid_taps(L.Ho, L.k, L.s, L.p, L.d, L.H) * valid_taps(L.Wo, L.k, L.s, L.p, L.d, L.W)
         nb = L.N * L.C * L.H * L.W * es + L.N * L.OC * L.Ho * L.Wo * es + L.OC * (L.k * L.k + 2) * es
+        return [("fwd", nb + (L.OC * es if L.bias else 0), fma, 1)]
+    if isinstance(L, WL.CachedLayer):
+        # bytes: x and y, plus the filter cache every call reads (the filter
+        # itself where the shape has no cached form)
+        from depthwise_convolution_dwconv2d_gb300 import binding as B
+        fma = L.N * L.OC * valid_taps(L.Ho, L.k, L.s, L.p, L.d, L.H) * valid_taps(L.Wo, L.k, L.s, L.p, L.d, L.W)
+        cache = B.dwconv2d_filter_cache_size(B.make_desc(**L.desc_kwargs()), 0)
+        nb = L.N * L.C * L.H * L.W * es + L.N * L.OC * L.Ho * L.Wo * es + (cache or L.OC * L.k * L.k * es)
         return [("fwd", nb + (L.OC * es if L.bias else 0), fma, 1)]
     xb = L.N * L.C * L.H * L.W * es
     yb = L.N * L.OC * L.Ho * L.Wo * es
@@ -342,6 +361,10 @@ def oracle_sample(items, budget_s):
                 t0 = time.perf_counter()
                 oracle.fwd_epilogue(cv, inp.x.f64, inp.w.f64, b, sc.f64, sh.f64, L.act)
                 t_total += time.perf_counter() - t0
+            elif isinstance(L, WL.CachedLayer):
+                t0 = time.perf_counter()
+                oracle.fwd(cv, inp.x.f64, inp.w.f64, b)
+                t_total += time.perf_counter() - t0
             else:
                 t0 = time.perf_counter()
                 oracle.fwd(cv, inp.x.f64, inp.w.f64, b)
@@ -370,6 +393,7 @@ def oracle_sample(items, budget_s):
         t, by, fm = run(n, c)
     passes = ("separable block (depthwise + 1x1, both epilogues)" if all(isinstance(i, WL.SepLayer) for i in items)
               else "fwd with epilogue" if all(isinstance(i, WL.InferLayer) for i in items)
+              else "fwd" if all(isinstance(i, WL.CachedLayer) for i in items)
               else "fwd+bwd_data+bwd_weight")
     desc = (f"first {n} sample(s)" + ("" if c >= full_c else f" and first {c} channels") +
             f" of every layer, {passes}, one timed pass")
@@ -511,6 +535,27 @@ def setup_workload(name, items, dev, stream, hc, out_host):
                           B.dwconv2d_fwd_nhwc(d, x, w, None, y, sc, sh, act, stream)))
             h2d = [(xh, x), (wh, w), (sch, sc), (shh, sh)]
             groups.append((h2d, list(range(idx0, len(calls))), [(y, host_out(y))]))
+            continue
+        if isinstance(L, WL.CachedLayer):
+            xh = hc.get(("x", (L.N, L.C, L.H, L.W), L.dtype, xd), lambda L=L: WL.make_x(L))
+            wh = hc.get(("w", (L.OC, L.k, L.k), L.dtype, 0, wstd), lambda L=L: WL.make_w(L))
+            d = B.make_desc(**L.desc_kwargs())
+            x, w = xh.to(dev), wh.to(dev)
+            y = torch.empty((L.N, L.OC, L.Ho, L.Wo), dtype=tdt(L.dtype), device=dev)
+            cl = layer_calls(L)
+            idx0 = len(calls)
+            nbytes = B.dwconv2d_filter_cache_size(d, 0)
+            if nbytes:
+                # static filter: its cache is built once, outside the timed calls
+                cache = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+                B.dwconv2d_filter_cache_build(d, 0, w, cache, None, stream)
+                calls.append(("fwd", L.label(), fam("ibgemm-cached", L.dtype), cl[0][1], cl[0][2], 1,
+                              lambda d=d, x=x, cache=cache, y=y: B.dwconv2d_fwd_cached(d, x, cache, None, y, None,
+                                                                                      stream)))
+            else:
+                calls.append(("fwd", L.label(), fam(B.dwconv2d_plan_name(d, 0), L.dtype), cl[0][1], cl[0][2], 1,
+                              lambda d=d, x=x, w=w, y=y: B.dwconv2d_fwd(d, x, w, None, y, stream)))
+            groups.append(([(xh, x)], list(range(idx0, len(calls))), [(y, host_out(y))]))
             continue
         xh = hc.get(("x", (L.N, L.C, L.H, L.W), L.dtype, xd), lambda L=L: WL.make_x(L))
         wh = hc.get(("w", (L.OC, L.k, L.k), L.dtype, 0, wstd), lambda L=L: WL.make_w(L))
@@ -696,7 +741,7 @@ def time_workload(name, items, args, dev, stream, world, dist, peaks, fma_tflops
     for key, f in fams.items():
         pass_, plan, dt = key.split(":")
         family = plan.replace("multi-", "")
-        if family in ("ibgemm", "tcwgrad", "septc"):
+        if family in ("ibgemm", "tcwgrad", "septc", "ibgemm-cached"):
             bp = ("tensor", tc_peak, tc_src)
         elif fma_tflops:
             bp = ("alu", fma_tflops, fma_src)
@@ -711,7 +756,7 @@ def time_workload(name, items, args, dev, stream, world, dist, peaks, fma_tflops
                   "share": round(f["ms"] / ms_per_step, 4)})
         rl[key] = r
     dom = max(fams, key=lambda k: fams[k]["ms"])
-    unit = "TFLOP/s" if name == "largek" else "GB/s"
+    unit = "TFLOP/s" if name in ("largek", "largek_infer") else "GB/s"
 
     def metric_of(ms):
         return (world * 2 * step_fma / ms / 1e9) if unit == "TFLOP/s" else (world * step_bytes / ms / 1e6)
@@ -798,7 +843,7 @@ def main():
     head = HEADLINE if HEADLINE in names else names[0]
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
-    unit_of = lambda n: "TFLOP/s" if n == "largek" else "GB/s"
+    unit_of = lambda n: "TFLOP/s" if n in ("largek", "largek_infer") else "GB/s"
 
     if args.impl == "reference":
         if rank != 0:

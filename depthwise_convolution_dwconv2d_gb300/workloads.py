@@ -140,6 +140,19 @@ def largek(N=64, C=384, sizes=(32, 48, 64), ks=(7, 13, 21, 27, 31), dtypes=("f32
             for dt in dtypes for h in sizes for k in ks]
 
 
+@dataclass
+class CachedLayer(Layer):
+    """A forward-only large-kernel layer whose filter is fixed across calls
+    (inference): served from a filter cache built once ahead of the calls
+    where the shape has a cached form, else by the uncached forward."""
+    cached: bool = True
+
+
+def largek_infer(N=64, C=384, sizes=(32, 48, 64), ks=(13, 21, 27, 31), dtype="f16"):
+    return [CachedLayer(N=N, C=C, H=h, W=h, k=k, s=1, p=k // 2, dtype=dtype, name=f"lki_H{h}_k{k}_{dtype}")
+            for h in sizes for k in ks]
+
+
 def multidil(N=2, C=64, H=256):
     return Multi(N=N, C=C, H=H, W=H)
 
