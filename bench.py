@@ -88,7 +88,7 @@ FAMILY_SOURCES = {
              "tile_wgrad_impl.cuh", "tile_multi.cu", "generic.cu"),
     "plane": ("common.cuh", "plan.h", "plane.cu", "generic.cu"),
     "large": ("common.cuh", "plan.h", "tile.cuh", "large.cu", "large_entries.h", "large_common.cuh",
-              "large_pair.cuh", "large_impl.cuh", "generic.cu"),
+              "large_pair.cuh", "large_impl.cuh", "large_pwgrad.cuh", "generic.cu"),
     "ibgemm": ("common.cuh", "plan.h", "tma.cuh", "tma.cu", "ibgemm.cu"),
     "tcwgrad": ("common.cuh", "plan.h", "tma.cuh", "tma.cu", "wgrad_tc.cu", "generic.cu"),
     "generic": ("common.cuh", "plan.h", "generic.cu"),

@@ -16,9 +16,10 @@ bool supported(const Conv& c) {
   return true;
 }
 
-// The weight gradient stages a padded x plane and a grad_out plane per stage,
-// two stages (fp32, whatever the storage type); its planner gives up above
-// 220 KB. This asks the same planner, on the shape alone.
+// The weight gradient's planner decides on the shape alone whether its
+// stages fit (the scalar kernel: a padded x plane and a grad_out plane per
+// stage, two stages, at most 220 KB; the packed kernel cuts the plane into
+// bands of output rows until they fit).
 bool wgrad_supported(const Conv& c) {
   if (!supported(c)) return false;
 #define X(K) \
@@ -45,14 +46,42 @@ cudaError_t bwd_data(const Conv& c, const void* gy, const void* w, void* gx, boo
   return cudaErrorInvalidConfiguration;
 }
 
-// Batch chunks of the weight gradient: about eight (channel, chunk) units per
-// resident CTA (two per SM), so the persistent CTAs end close together.
+// Partials per channel of the weight gradient (the planner's "chunks"):
+// sample chunks for the scalar kernel, sample chunks x bands of output rows
+// for the packed one. Depends on the descriptor alone.
 int wgrad_chunks(const Conv& c) {
+#define X(K) \
+  if (c.kh == K) return wgrad_parts_k##K(c);
+  DW_LARGE_SIZES(X)
+#undef X
+  return 1;
+}
+
+// Sample chunks of the scalar weight gradient (also the tensor-core weight
+// gradient's chunks): about eight (channel, chunk) units per resident CTA.
+int sample_chunks(const Conv& c) {
   int64_t chunks = (152 * 2 * 8 + c.C - 1) / c.C;
   if (chunks > c.N) chunks = c.N;
   if (chunks < 1) chunks = 1;
   const int64_t nb = (c.N + chunks - 1) / chunks;
   return (int)(c.N > 0 ? (c.N + nb - 1) / nb : 1);
+}
+
+bool wgrad_scalar_supported(const Conv& c) {
+  if (!supported(c)) return false;
+#define X(K) \
+  if (c.kh == K) return wgrad_scalar_fits_k##K(c);
+  DW_LARGE_SIZES(X)
+#undef X
+  return false;
+}
+
+cudaError_t wgrad_scalar(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s) {
+#define X(K) \
+  if (c.kh == K) return wgrad_scalar_k##K(c, x, gy, ws, chunks, s);
+  DW_LARGE_SIZES(X)
+#undef X
+  return cudaErrorInvalidConfiguration;
 }
 
 cudaError_t wgrad(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s) {

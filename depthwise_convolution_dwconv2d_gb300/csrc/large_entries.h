@@ -13,9 +13,13 @@ namespace large {
   cudaError_t fwd_k##K(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s,   \
                        const Epi& ep);                                                                      \
   cudaError_t bwd_k##K(const Conv& c, const void* gy, const void* w, void* gx, bool acc, cudaStream_t s);   \
-  cudaError_t wgrad_k##K(const Conv& c, const void* x, const void* gy, float* ws, int chunks,              \
+  cudaError_t wgrad_k##K(const Conv& c, const void* x, const void* gy, float* ws, int parts,               \
                          cudaStream_t s);                                                                   \
-  bool wgrad_fits_k##K(const Conv& c);
+  int wgrad_parts_k##K(const Conv& c);                                                                      \
+  bool wgrad_fits_k##K(const Conv& c);                                                                      \
+  cudaError_t wgrad_scalar_k##K(const Conv& c, const void* x, const void* gy, float* ws, int chunks,       \
+                                cudaStream_t s);                                                            \
+  bool wgrad_scalar_fits_k##K(const Conv& c);
 DW_LARGE_SIZES(DW_LARGE_DECLARE)
 #undef DW_LARGE_DECLARE
 

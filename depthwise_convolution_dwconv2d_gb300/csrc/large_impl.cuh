@@ -8,6 +8,7 @@
 
 #include "large_common.cuh"
 #include "large_pair.cuh"
+#include "large_pwgrad.cuh"
 
 namespace dwconv {
 namespace large {
@@ -360,8 +361,31 @@ cudaError_t run_wgrad_k(const Conv& c, const void* x, const void* gy, float* ws,
   return cudaGetLastError();
 }
 
+// Weight-gradient kernel per filter size: the packed sample-pair kernel
+// (large_pwgrad.cuh) for 15 to 21 taps, where it is faster (10-15 % at 21 on
+// 32..64-row planes); the scalar kernel above elsewhere: from 23 taps the
+// packed kernel's register ring and per-row bookkeeping cost more than its
+// halved issue slots save, and at 13 taps and below the two are level.
+template <int K>
+constexpr bool kPackedWgrad = K >= 15 && K <= 21;
+
+// Batch chunks of the scalar weight gradient: about eight (channel, chunk)
+// units per resident CTA (two per SM), so the persistent CTAs end close
+// together.
+inline int scalar_wgrad_chunks(const Conv& c) {
+  int64_t chunks = (152 * 2 * 8 + c.C - 1) / c.C;
+  if (chunks > c.N) chunks = c.N;
+  if (chunks < 1) chunks = 1;
+  const int64_t nb = (c.N + chunks - 1) / chunks;
+  return (int)(c.N > 0 ? (c.N + nb - 1) / nb : 1);
+}
+
 // Per-K entry points: one translation unit per K (large_kNN.cu) defines them
-// with this macro; large_entries.h declares them.
+// with this macro; large_entries.h declares them. wgrad_parts_kK is the
+// number of partials per channel the weight gradient writes (the second
+// pass sums them); the wgrad_scalar_* entries run the scalar kernel over
+// sample chunks whatever K is (the fallback of the tensor-core weight
+// gradient, which chunks the batch the same way).
 #define DW_LARGE_DEFINE(K)                                                                                   \
   cudaError_t fwd_k##K(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s,   \
                        const Epi& ep) {                                                                     \
@@ -370,11 +394,24 @@ cudaError_t run_wgrad_k(const Conv& c, const void* x, const void* gy, float* ws,
   cudaError_t bwd_k##K(const Conv& c, const void* gy, const void* w, void* gx, bool acc, cudaStream_t s) {  \
     return run_fwd_k<K>(c, gy, w, nullptr, gx, true, acc, s, Epi{});                                        \
   }                                                                                                         \
-  cudaError_t wgrad_k##K(const Conv& c, const void* x, const void* gy, float* ws, int chunks,              \
+  cudaError_t wgrad_k##K(const Conv& c, const void* x, const void* gy, float* ws, int parts,               \
                          cudaStream_t s) {                                                                  \
+    if constexpr (kPackedWgrad<K>) return run_pwgrad_k<K>(c, x, gy, ws, parts, s);                         \
+    else return run_wgrad_k<K>(c, x, gy, ws, parts, s);                                                     \
+  }                                                                                                         \
+  int wgrad_parts_k##K(const Conv& c) {                                                                     \
+    if constexpr (kPackedWgrad<K>) return pwgrad_parts<K>(c);                                               \
+    else return scalar_wgrad_chunks(c);                                                                     \
+  }                                                                                                         \
+  bool wgrad_fits_k##K(const Conv& c) {                                                                     \
+    if constexpr (kPackedWgrad<K>) return plan_pwgrad<K>(c, nullptr, nullptr);                              \
+    else return plan_wgrad<K>(c, 1, nullptr, nullptr);                                                      \
+  }                                                                                                         \
+  cudaError_t wgrad_scalar_k##K(const Conv& c, const void* x, const void* gy, float* ws, int chunks,       \
+                                cudaStream_t s) {                                                           \
     return run_wgrad_k<K>(c, x, gy, ws, chunks, s);                                                         \
   }                                                                                                         \
-  bool wgrad_fits_k##K(const Conv& c) { return plan_wgrad<K>(c, 1, nullptr, nullptr); }
+  bool wgrad_scalar_fits_k##K(const Conv& c) { return plan_wgrad<K>(c, 1, nullptr, nullptr); }
 
 }  // namespace large
 }  // namespace dwconv

@@ -60,7 +60,7 @@ Algo plan_bwd_data(const Conv& c) {
 WPlan plan_bwd_weight(const Conv& c) {
   if (!force_generic() && plane::wgrad_supported(c)) return WPlan{Algo::Plane, plane::wgrad_chunks(c)};
   if (!force_generic() && tile::wgrad_supported(c)) return WPlan{Algo::Tile, tile::wgrad_chunks(c)};
-  if (!force_generic() && allow_ibgemm() && wtc::supported(c)) return WPlan{Algo::TcWgrad, large::wgrad_chunks(c)};
+  if (!force_generic() && allow_ibgemm() && wtc::supported(c)) return WPlan{Algo::TcWgrad, large::sample_chunks(c)};
   if (!force_generic() && large::wgrad_supported(c)) return WPlan{Algo::Large, large::wgrad_chunks(c)};
   // generic first pass: a chunk of whole samples per block, at most 2^20
   // positions per chunk so each thread's serial chain stays <= 4096 terms.
@@ -125,7 +125,7 @@ cudaError_t run_bwd_weight(const WPlan& p, const Conv& c, const void* x, const v
       // only; the direct kernels take the same chunks (same workspace)
       e = wtc::wgrad(c, x, gy, ws, p.chunks, s);
       if (e == cudaErrorNotSupported)
-        e = large::wgrad_supported(c) ? large::wgrad(c, x, gy, ws, p.chunks, s)
+        e = large::wgrad_scalar_supported(c) ? large::wgrad_scalar(c, x, gy, ws, p.chunks, s)
                                       : bwd_weight_generic_pass1(c, x, gy, ws, p.chunks, gw != nullptr, gb != nullptr, s);
       break;
     default:

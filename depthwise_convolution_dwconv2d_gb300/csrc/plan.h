@@ -71,8 +71,13 @@ bool wgrad_supported(const Conv& c);  // supported() and the weight-gradient sta
 cudaError_t fwd(const Conv& c, const void* x, const void* w, const void* b, void* y, cudaStream_t s,
                 const Epi& ep = Epi{});
 cudaError_t bwd_data(const Conv& c, const void* gy, const void* w, void* gx, bool acc, cudaStream_t s);
-int wgrad_chunks(const Conv& c);
+int wgrad_chunks(const Conv& c);  // partials per channel of wgrad()
 cudaError_t wgrad(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s);
+// the scalar weight gradient over sample chunks, for any K (fallback of the
+// tensor-core weight gradient, which uses the same chunks)
+int sample_chunks(const Conv& c);
+bool wgrad_scalar_supported(const Conv& c);
+cudaError_t wgrad_scalar(const Conv& c, const void* x, const void* gy, float* ws, int chunks, cudaStream_t s);
 }  // namespace large
 
 namespace plane {

@@ -166,5 +166,47 @@ def test_cache_rebuild_follows_the_filter():
     assert_close(to_f64(y2), oracle.fwd(oconv(L2), x2.f64, i2.w.f64, None), "f16", L.k * L.k, "other N and H")
 
 
+_FULL = {}
+
+
+def _full_inputs(L):
+    """x and grad_out of a full-size layer depend only on (H, dtype) here;
+    keep the most recent pair."""
+    key = (L.H, L.dtype)
+    if key not in _FULL:
+        _FULL.clear()
+        _FULL[key] = WL.make_inputs(WL.Layer(N=L.N, C=L.C, H=L.H, W=L.W, k=1, p=0, dtype=L.dtype))
+    return _FULL[key]
+
+
+@pytest.mark.parametrize("L", [L for L in WL.largek_infer() if L.H in (32, 64) and (L.H == 32 or L.k <= 21)],
+                         ids=lambda L: L.name)
+def test_cached_full_size_sampled(L):
+    """The benchmark's full-size layers (64 x 384) in the launch configuration
+    the bench times: cached forward and grad-input, oracle on sampled planes
+    (edge and interior samples and channels: the persistent units straddle
+    channels and tile groups)."""
+    th = torch()
+    d = B.make_desc(**L.desc_kwargs())
+    assert B.dwconv2d_filter_cache_size(d, 0) > 0
+    inp = _full_inputs(L)
+    w = synth.normal_tensor((L.OC, L.k, L.k), L.dtype, 0, synth.STREAM_W, std=1.0 / L.k)
+    wd = to_dev(w)
+    y = empty_dev((L.N, L.C, L.Ho, L.Wo), L.dtype)
+    B.dwconv2d_fwd_cached(d, to_dev(inp.x), cache_for(d, 0, wd), None, y)
+    gx = empty_dev((L.N, L.C, L.H, L.W), L.dtype)
+    B.dwconv2d_bwd_data_cached(d, to_dev(inp.gy), cache_for(d, 1, wd), gx, 0)
+    th.cuda.synchronize()
+    nsel, csel = [0, 31, 63], [0, 1, 191, 383]
+    cv = oconv(L, N=len(nsel), C=len(csel))
+    xs = inp.x.f64[np.ix_(nsel, csel)]
+    gys = inp.gy.f64[np.ix_(nsel, csel)]
+    ws = w.f64[csel]
+    taps = L.k * L.k
+    assert_close(to_f64(y)[np.ix_(nsel, csel)], oracle.fwd(cv, xs, ws, None), L.dtype, taps, f"{L.name} cached fwd")
+    assert_close(to_f64(gx)[np.ix_(nsel, csel)], oracle.bwd_data(cv, gys, ws), L.dtype, taps,
+                 f"{L.name} cached bwd_data")
+
+
 def test_no_bounded_wait_gave_up_after_cached_calls():
     assert B.dwconv_device_timeouts() == 0
