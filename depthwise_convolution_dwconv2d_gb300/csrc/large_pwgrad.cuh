@@ -38,10 +38,9 @@ namespace large {
 
 template <int K>
 struct PWGeo {
-  // four filter rows per thread for the largest filters (8 row blocks, 8
-  // groups, one CTA per SM with room for the larger register ring), three
-  // for the rest (two CTAs per SM)
-  static constexpr int RA = K >= 29 ? 4 : 3, VB = 8;
+  // three filter rows per thread (two CTAs per SM; four rows, with one CTA
+  // per SM for the larger register ring, measured slower)
+  static constexpr int RA = 3, VB = 8;
   static constexpr int min_ctas = RA == 4 ? 1 : 2;
   static constexpr int NA = (K + RA - 1) / RA, NB = (K + VB - 1) / VB;
   static constexpr int items = NA * NB;

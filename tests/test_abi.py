@@ -276,14 +276,14 @@ def test_tile_routing_respects_band_limits(lib):
 
 
 def test_large_weight_gradient_routing_respects_shared_memory(lib):
-    """The scalar large-filter weight gradient (outside 15..21 taps) stages two
+    """The scalar large-filter weight gradient (outside 15..27 taps) stages two
     fp32 (x tile + grad_out plane) stages; from 112 x 112 planes it would
-    need more than its 220 KB limit (k = 25 at 112 x 112: 2 x (139 rows x 148
-    + 112 x 112) floats = 265 KB), so those shapes take the generic weight
+    need more than its 220 KB limit (k = 29 at 112 x 112: 2 x (143 rows x 148
+    + 112 x 112) floats = 270 KB), so those shapes take the generic weight
     gradient while the forward and grad-input stay on the large kernels. The
-    packed kernel (15 to 21 taps) cuts a plane into bands of output rows
+    packed kernel (15 to 27 taps) cuts a plane into bands of output rows
     until they fit, so it serves them."""
-    big = B.make_desc(4, 8, 112, 112, 25, 1, 12)
+    big = B.make_desc(4, 8, 112, 112, 29, 1, 14)
     assert B.dwconv2d_plan_name(big, 0) == "large"
     assert B.dwconv2d_plan_name(big, 2) == "generic"
     banded = B.make_desc(4, 8, 112, 112, 17, 1, 8)
