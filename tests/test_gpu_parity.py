@@ -380,12 +380,13 @@ BANDED_WGRAD = [
     WL.Layer(N=2, C=3, H=128, W=120, k=21, p=10, dtype="f32", name="k21H128W120_f32"),
     WL.Layer(N=5, C=2, H=100, W=97, k=19, p=3, dtype="bf16", name="k19H100W97p3_bf16"),
     WL.Layer(N=2, C=3, H=112, W=100, k=27, p=13, bias=True, dtype="f32", name="k27H112W100_f32"),
+    WL.Layer(N=3, C=2, H=120, W=72, k=31, p=9, dtype="f16", name="k31H120W72p9_f16"),
 ]
 
 
 @pytest.mark.parametrize("L", BANDED_WGRAD, ids=lambda L: L.name)
 def test_large_weight_gradient_banded_planes(L):
-    """The packed large weight gradient (15 to 27 taps) on planes it cuts into
+    """The packed large weight gradient (15 taps and up) on planes it cuts into
     bands of output rows (112..128 rows), with bias, a ragged odd width and
     non-"same" padding, against the oracle."""
     os.environ["DWCONV_FORCE_ALGO"] = "direct"
