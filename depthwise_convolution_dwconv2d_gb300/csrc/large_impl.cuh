@@ -362,11 +362,11 @@ cudaError_t run_wgrad_k(const Conv& c, const void* x, const void* gy, float* ws,
 }
 
 // Weight-gradient kernel per filter size: the packed sample-pair kernel
-// (large_pwgrad.cuh) from 15 taps, where it is faster (10-15 % at 21, 4-7 %
-// at 27, 6-13 % at 31 on 32..64-row planes); the scalar kernel above up to
-// 13 taps, where the two are level.
+// (large_pwgrad.cuh) from 13 taps, where it is faster (6-13 % at 13 and 31,
+// 10-15 % at 21, 4-7 % at 27 on 32..64-row planes); the scalar kernel above
+// below 13 taps.
 template <int K>
-constexpr bool kPackedWgrad = K >= 15;
+constexpr bool kPackedWgrad = K >= 13;
 
 // Batch chunks of the scalar weight gradient: about eight (channel, chunk)
 // units per resident CTA (two per SM), so the persistent CTAs end close

@@ -38,11 +38,12 @@ namespace large {
 
 template <int K>
 struct PWGeo {
-  // three filter rows per thread up to 27 taps, two from 29 (31 taps in
-  // blocks of three would leave the last block one row of three and only
-  // five row groups per CTA; four rows, with one CTA per SM for the larger
-  // register ring, measured slower as well); two CTAs per SM
-  static constexpr int RA = K >= 29 ? 2 : 3, VB = 8;
+  // three filter rows per thread where three divide K (no empty rows in
+  // the last block), else two (measured at 13, 21, 27 and 31 taps: two rows
+  // are 2-8 % slower at 21 and 27, three rows 11-16 % slower at 31, where
+  // the last block holds one row of three and only five row groups fit a
+  // CTA; four rows with one CTA per SM were slower still); two CTAs per SM
+  static constexpr int RA = K % 3 == 0 ? 3 : 2, VB = 8;
   static constexpr int min_ctas = RA == 4 ? 1 : 2;
   static constexpr int NA = (K + RA - 1) / RA, NB = (K + VB - 1) / VB;
   static constexpr int items = NA * NB;

@@ -276,12 +276,12 @@ def test_tile_routing_respects_band_limits(lib):
 
 
 def test_large_weight_gradient_routing_respects_shared_memory(lib):
-    """The scalar large-filter weight gradient (up to 13 taps) stages two fp32
+    """The scalar large-filter weight gradient (below 13 taps) stages two fp32
     (x tile + grad_out plane) stages; from 112 x 112 planes it would need
     more than its 220 KB limit (k = 9 at 112 x 112: 2 x (123 rows x 132 +
     112 x 112) floats = 230 KB), so those shapes take the generic weight
     gradient while the forward and grad-input stay on the large kernels. The
-    packed kernel (15 taps and up) cuts a plane into bands of output rows
+    packed kernel (13 taps and up) cuts a plane into bands of output rows
     until they fit, so it serves them."""
     big = B.make_desc(4, 8, 112, 112, 9, 1, 4)
     assert B.dwconv2d_plan_name(big, 0) == "large"

@@ -386,7 +386,7 @@ BANDED_WGRAD = [
 
 @pytest.mark.parametrize("L", BANDED_WGRAD, ids=lambda L: L.name)
 def test_large_weight_gradient_banded_planes(L):
-    """The packed large weight gradient (15 taps and up) on planes it cuts into
+    """The packed large weight gradient (13 taps and up) on planes it cuts into
     bands of output rows (112..128 rows), with bias, a ragged odd width and
     non-"same" padding, against the oracle."""
     os.environ["DWCONV_FORCE_ALGO"] = "direct"
