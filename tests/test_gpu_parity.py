@@ -259,8 +259,10 @@ def test_delta_kernel_bit_exact(dtype, k, s, d):
 
 @pytest.mark.parametrize("L", [WL.mobilenet(N=4)[1], WL.mobilenet(N=4)[0],
                                WL.Layer(N=2, C=8, H=33, W=35, k=5, p=2, m=2, bias=True, dtype="bf16"),
-                               WL.Layer(N=2, C=4, H=40, W=40, k=13, p=6, dtype="f16")],
-                         ids=["s1", "s2", "m2bf16", "k13f16"])
+                               WL.Layer(N=2, C=4, H=40, W=40, k=13, p=6, dtype="f16"),
+                               WL.Layer(N=3, C=4, H=40, W=36, k=21, p=10, bias=True, dtype="f32"),
+                               WL.Layer(N=2, C=3, H=34, W=34, k=31, p=15, dtype="f32")],
+                         ids=["s1", "s2", "m2bf16", "k13f16", "k21f32", "k31f32"])
 def test_slice_guard_bands_and_accumulate(L):
     """Channels outside the slice stay bit-identical; accumulate adds."""
     th = torch()
