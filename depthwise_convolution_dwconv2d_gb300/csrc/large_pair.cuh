@@ -438,6 +438,16 @@ bool plan_pair(const Conv& c, bool flip, PCfg* out_cfg, int* threads_out, double
     if (ppu < 1) continue;
     t.ppu = (int)ppu;
     t.items = (int)(ppu * ipb);
+    // rows in mirror order (a warp's lanes then share equal filter-row
+    // ranges) unless a quarter-warp's items wrap from one row to the next
+    // and the filter is long: a mirror partner sits at a row distance that
+    // changes from one quarter-warp to the next, so no row stride keeps
+    // their window loads apart (at 48 columns a third of the shared-memory
+    // wavefronts were conflicts), while the next row in plain order is
+    // always one stride away. Measured on the 64 x 384 layers: plain order
+    // 2-5 % faster at 48 rows for 21..31 taps, 2-4 % slower at 13 taps,
+    // where the unequal ranges at the plane edges weigh more.
+    if (((int64_t)t.ppu * g.cb) % 8 != 0 && K >= 21) t.mirror = 0;
     const int threads = ((t.items < kNT ? t.items : kNT) + 31) / 32 * 32;
     // strides with the fewest bank-group conflicts among those that keep the
     // unit within the limit: row stride first, then the block stride
