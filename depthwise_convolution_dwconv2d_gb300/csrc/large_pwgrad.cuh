@@ -338,13 +338,21 @@ int pw_conflicts(const PWCfg& g, int threads) {
   return total;
 }
 
-// Batch chunks of the sample axis: about eight (channel, chunk) units per
-// resident CTA (two per SM), so the persistent CTAs end close together.
-inline int pw_chunks(const Conv& c) {
+// Samples per chunk of the sample axis: about eight (channel, chunk) units
+// per resident CTA (two per SM), so the persistent CTAs end close together,
+// rounded up to an even count so that only the batch's last sample can sit
+// in a half-empty pair (a chunk of 3 samples would spend a quarter of its
+// FMAs on the zero second lane of its last pair).
+inline int64_t pw_chunk_samples(const Conv& c) {
   int64_t chunks = (152 * 2 * 8 + c.C - 1) / c.C;
   if (chunks > c.N) chunks = c.N;
   if (chunks < 1) chunks = 1;
   const int64_t nb = (c.N + chunks - 1) / chunks;
+  return nb + (nb & 1);
+}
+
+inline int pw_chunks(const Conv& c) {
+  const int64_t nb = pw_chunk_samples(c);
   return (int)(c.N > 0 ? (c.N + nb - 1) / nb : 1);
 }
 
@@ -359,7 +367,7 @@ bool plan_pwgrad(const Conv& c, PWCfg* out_cfg, size_t* smem_out) {
   const int Ho = (int)c.Ho, Wo = (int)c.Wo;
   PWCfg g{};
   g.chunks = pw_chunks(c);
-  g.nb = (int)(c.N > 0 ? (c.N + g.chunks - 1) / g.chunks : 1);
+  g.nb = (int)(c.N > 0 ? pw_chunk_samples(c) : 1);
   g.pad = c.ph;
   g.dtype = c.dtype;
   g.gcols = (Wo + 1) / 2 * 2;
