@@ -607,6 +607,28 @@ def roofline_of(fam_rec, bound_peaks, hbm_peak, hbm_kind, traffic_entry):
             "compute_frac": round(2 * fma / ms / 1e9 / comp_peak, 4)}
 
 
+def max_over_ranks(vals, dist, device="cpu"):
+    """Per-rank timings (ms; None for "not measured") -> their maximum over
+    all ranks, the same list on every rank. With one rank (dist None) the
+    values come back unchanged."""
+    if dist is None:
+        return list(vals)
+    import torch
+
+    t = torch.tensor([float(v) if v is not None else 0.0 for v in vals], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) if float(x) > 0.0 else None for x in t]
+
+
+def job_throughput(world, step_units, ms, unit):
+    """Whole-job throughput: every rank runs one replica of the step, so the
+    units all ranks processed (world x one step's bytes or valid-tap FMAs)
+    over the slowest rank's step time."""
+    if unit == "TFLOP/s":
+        return world * 2 * step_units / ms / 1e9
+    return world * step_units / ms / 1e6
+
+
 def time_workload(name, items, args, dev, stream, world, dist, peaks, fma_tflops):
     import torch
     from depthwise_convolution_dwconv2d_gb300 import binding as B
@@ -712,10 +734,7 @@ def time_workload(name, items, args, dev, stream, world, dist, peaks, fma_tflops
         h2d_bytes = sum(h.numel() * h.element_size() for g in groups for h, _ in g[0])
         d2h_bytes = sum(h.numel() * h.element_size() for g in groups for _, h in g[2])
 
-    if dist is not None:
-        t = torch.tensor([ms_per_step, e2e_ms or 0.0], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step, e2e_ms = float(t[0]), (float(t[1]) or None)
+    ms_per_step, e2e_ms = max_over_ranks([ms_per_step, e2e_ms], dist, dev)
 
     hbm_peak, hbm_kind, tc_peak, tc_kind = peaks
     fams = {}
@@ -760,15 +779,15 @@ def time_workload(name, items, args, dev, stream, world, dist, peaks, fma_tflops
     unit = "TFLOP/s" if name in ("largek", "largek_infer") else "GB/s"
 
     def metric_of(ms):
-        return (world * 2 * step_fma / ms / 1e9) if unit == "TFLOP/s" else (world * step_bytes / ms / 1e6)
+        return job_throughput(world, step_fma if unit == "TFLOP/s" else step_bytes, ms, unit)
 
     dts = sorted({getattr(i, "dtype", "f32") for i in items}, key=lambda d: ("f32", "f16", "bf16").index(d))
     rec = {
         "workload": WORKLOAD_TEXT[name], "name": name,
         "value": round(metric_of(ms_per_step), 3), "unit": unit,
         "ms_per_step": round(ms_per_step, 4),
-        "GBps": round(world * step_bytes / ms_per_step / 1e6, 1),
-        "TFLOPs_valid": round(world * 2 * step_fma / ms_per_step / 1e9, 3),
+        "GBps": round(job_throughput(world, step_bytes, ms_per_step, "GB/s"), 1),
+        "TFLOPs_valid": round(job_throughput(world, step_fma, ms_per_step, "TFLOP/s"), 3),
         "dtype": "+".join(dts),
         "step_bytes": step_bytes, "step_fma_valid": step_fma,
         "roofline": rl[dom],
