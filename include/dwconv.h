@@ -38,6 +38,11 @@
  *  - Work is enqueued on `stream` (0 = legacy default stream) and nothing
  *    waits for it. A launch failure returns DWCONV_ERR_CUDA; faults during
  *    execution surface at the caller's next synchronisation.
+ *  - Graph capture: a call enqueues only kernel launches on `stream` (no
+ *    allocation, copy, memset or synchronisation, no other stream), so calls
+ *    on a capturing stream are recorded into the caller's CUDA graph and
+ *    give bitwise the same results on replay. (dwconv2d_bwd_weight_noalloc:
+ *    make its first call on a device outside any capture, see below.)
  *  - Errors: arguments are checked on the host before any launch; on any
  *    error nothing is enqueued and nothing is written. Nothing prints or aborts.
  *  - Alignment: each pointer must be aligned to its element size
