@@ -38,11 +38,15 @@
  *  - Work is enqueued on `stream` (0 = legacy default stream) and nothing
  *    waits for it. A launch failure returns DWCONV_ERR_CUDA; faults during
  *    execution surface at the caller's next synchronisation.
- *  - Graph capture: a call enqueues only kernel launches on `stream` (no
- *    allocation, copy, memset or synchronisation, no other stream), so calls
- *    on a capturing stream are recorded into the caller's CUDA graph and
- *    give bitwise the same results on replay. (dwconv2d_bwd_weight_noalloc:
- *    make its first call on a device outside any capture, see below.)
+ *  - Graph capture: a compute call (every entry point that takes a stream;
+ *    dwconv_device_timeouts is a synchronous read) enqueues only kernel
+ *    launches on `stream` (no allocation, copy, memset or synchronisation,
+ *    no other stream), so calls on a capturing stream are recorded into the
+ *    caller's CUDA graph and give bitwise the same results on replay. Make
+ *    the first call of a shape and entry point on a device outside any
+ *    capture: it sets the kernels' shared-memory limits and looks up device
+ *    addresses (for dwconv2d_bwd_weight_noalloc this is required, see
+ *    below).
  *  - Errors: arguments are checked on the host before any launch; on any
  *    error nothing is enqueued and nothing is written. Nothing prints or aborts.
  *  - Alignment: each pointer must be aligned to its element size
