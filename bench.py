@@ -176,6 +176,26 @@ def layer_calls(item):
             ("bwd_weight", xb + yb + wb + bb, fma, 2)]
 
 
+def dense_fma(item):
+    """One step's dense tap count of a workload item, the pages' convention:
+    every output times every filter tap (N*OC*Ho*Wo*kh*kw per pass, padded
+    taps included), beside the valid-tap count the roofline uses. The 1x1
+    stage of a separable block has no padding: its MACs count the same in
+    both."""
+    from depthwise_convolution_dwconv2d_gb300 import workloads as WL
+    if isinstance(item, WL.Multi):
+        brs, _ = item.branches()
+        per = sum(L.N * L.OC * L.Ho * L.Wo * L.k * L.k for L in brs)
+        return 3 * per  # fwd, bwd_data (branch sum), bwd_weight per branch
+    L = item
+    per = L.N * L.OC * L.Ho * L.Wo * L.k * L.k
+    if isinstance(L, WL.SepLayer):
+        return per + L.N * L.Ho * L.Wo * L.OC * L.cout
+    if isinstance(L, (WL.InferLayer, WL.CachedLayer)):
+        return per
+    return 3 * per
+
+
 # ------------------------------------------------------------------ helpers
 def load_peaks():
     """(HBM GB/s, its source, dense bf16 TFLOP/s burst, its source)."""
@@ -666,6 +686,7 @@ def time_workload(name, items, args, dev, stream, world, dist, peaks, fma_tflops
     torch.cuda.synchronize()
     step_bytes = sum(c[3] for c in calls)
     step_fma = sum(c[4] for c in calls)
+    step_fma_dense = sum(dense_fma(i) for i in items)
     launches_per_step = sum(c[5] for c in calls)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     # L2 flush before every timed call: write a buffer of 2x L2 (evicts the
@@ -826,6 +847,8 @@ def time_workload(name, items, args, dev, stream, world, dist, peaks, fma_tflops
         "TFLOPs_valid": round(job_throughput(world, step_fma, ms_per_step, "TFLOP/s"), 3),
         "dtype": "+".join(dts),
         "step_bytes": step_bytes, "step_fma_valid": step_fma,
+        "step_fma_dense": step_fma_dense, "valid_over_dense": round(step_fma / step_fma_dense, 4),
+        "TFLOPs_dense": round(job_throughput(world, step_fma_dense, ms_per_step, "TFLOP/s"), 3),
         "roofline": rl[dom],
         "roofline_by_family": rl,
         "passes": {k: {"ms": round(v["ms"], 4), "GBps": round(v["bytes"] / v["ms"] / 1e6, 1),
