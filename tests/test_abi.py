@@ -224,6 +224,27 @@ def test_plan_names(lib):
     assert B.dwconv2d_plan_name(B.make_desc(64, 128, 56, 56, 3, 1, 1), -1) == "invalid"
 
 
+def test_packed_weight_gradient_chunks_hold_whole_pairs(lib):
+    """Host planning of the packed fp32 large weight gradient (no GPU needed):
+    about eight (channel, chunk) units per resident CTA (two per SM on 152
+    SMs), chunks of an even number of samples so that only the batch's last
+    sample can sit in a half-empty pair; the workspace holds chunks x OC x
+    (k*k + 1) fp32 partials."""
+    K = 31
+    for N, C in [(16, 384), (64, 384), (33, 384), (9, 64), (7, 64), (1, 64), (2, 64), (200, 64)]:
+        d = B.make_desc(N, C, 32, 32, K, 1, K // 2, 1, 1, "f32")
+        assert B.dwconv2d_plan_name(d, 2) == "large"
+        per_chunk = C * (K * K + 1) * 4  # C a multiple of 64: a whole number of 256-byte blocks
+        ws = B.dwconv2d_bwd_weight_workspace_size(d)
+        assert ws % per_chunk == 0
+        chunks = ws // per_chunk
+        want = max(1, min((152 * 2 * 8 + C - 1) // C, N))
+        nb = (N + want - 1) // want
+        nb += nb & 1
+        assert chunks == (N + nb - 1) // nb, (N, C, chunks)
+        assert nb % 2 == 0 and (chunks - 1) * nb < N <= chunks * nb
+
+
 def test_plane_routing_and_chunking(lib):
     """Host planning of the small-plane family (no GPU needed): the forward and
     stride-1 grad-input take it on rows of 9..16, the weight gradient on

@@ -399,6 +399,24 @@ def test_large_weight_gradient_banded_planes(L):
         del os.environ["DWCONV_FORCE_ALGO"]
 
 
+ODD_BATCH_WGRAD = [
+    WL.Layer(N=1, C=3, H=40, W=40, k=31, p=15, dtype="f32", name="N1_k31"),
+    WL.Layer(N=9, C=40, H=32, W=32, k=31, p=15, bias=True, dtype="f32", name="N9C40_k31"),
+    WL.Layer(N=7, C=6, H=36, W=36, k=21, p=10, dtype="f32", name="N7_k21"),
+    WL.Layer(N=3, C=5, H=20, W=44, k=13, p=6, bias=True, dtype="f32", name="N3_k13W44"),
+]
+
+
+@pytest.mark.parametrize("L", ODD_BATCH_WGRAD, ids=lambda L: L.name)
+def test_packed_weight_gradient_odd_batches(L):
+    """The packed fp32 weight gradient walks samples in pairs over chunks of
+    an even number of samples; with an odd batch the last chunk ends in a
+    pair whose second sample is missing (zero-filled). One sample, nine
+    samples in chunks of two, seven, and three, against the oracle."""
+    assert B.dwconv2d_plan_name(desc_of(L), 2) == "large"
+    check_full(L, WL.make_inputs(L), L.label())
+
+
 def test_large_direct_accumulate_into_gx():
     """The stride-1 grad-input of the direct large kernels adds into gx when
     asked (accumulate = 1)."""
