@@ -58,9 +58,11 @@ CASES = [
     WL.Layer(N=300, C=2, H=8, W=8, k=11, p=5, bias=True, dtype="bf16"),
     WL.Layer(N=5, C=3, H=45, W=32, k=21, p=10, dtype="f16"),
     WL.Layer(N=33, C=2, H=96, W=64, k=13, p=6, bias=True, dtype="bf16"),
+    WL.Layer(N=1, C=3, H=32, W=32, k=27, p=13, bias=True, dtype="f16"),
+    WL.Layer(N=1, C=2, H=16, W=64, k=21, p=10, dtype="bf16"),
 ]
 IDS = ["k31f16_W32", "k13bf16_W16", "k9f16_W8_raggedM", "k21f16_W64_groups", "k15bf16_N130_chunks",
-       "k11bf16_N300", "k21f16_H45", "k13bf16_W64_H96"]
+       "k11bf16_N300", "k21f16_H45", "k13bf16_W64_H96", "k27f16_N1", "k21bf16_N1_W64"]
 
 
 def check(L, inp, label):
