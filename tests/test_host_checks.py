@@ -12,7 +12,11 @@ arithmetic the kernel's threads perform against the planned layout:
   * check_ibc.cu: the filter-cache tensor-core kernel: shared- and
     tensor-memory plan, the cache's strip taps, the K steps and strip
     offsets of every tile, and the whole GEMM walk equal to a direct integer
-    correlation.
+    correlation;
+  * check_ibgemm.cu: the uncached tensor-core forward / grad-input: memory
+    plan, K steps covering every input position a tile reads, and the
+    builders' 16-byte filter pieces (bounds, alignment, values) walked
+    against a direct integer correlation.
 Each prints one line per plan and exits non-zero on any failure.
 """
 import os
@@ -25,7 +29,7 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HOST = os.path.join(ROOT, "tests", "host")
 CSRC = os.path.join(ROOT, "depthwise_convolution_dwconv2d_gb300", "csrc")
-PROGRAMS = ["check_pair", "check_pwgrad", "check_ibc"]
+PROGRAMS = ["check_pair", "check_pwgrad", "check_ibc", "check_ibgemm"]
 
 
 @pytest.fixture(scope="module")
